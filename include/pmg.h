@@ -1,0 +1,180 @@
+/*
+ * pmg.h — C ABI of the GB300 paged MLA KV-cache gather.
+ *
+ * The operation is the one described in "MLA cache gather scheduled per
+ * logical page" (prhub.com.cn, vllm PR #51739). The binding it documents is
+ * ops.cp_gather_cache(src_cache, dst, block_table, cu_seq_lens, batch_size,
+ * seq_starts) (section "关键源码片段", test
+ * test_cp_gather_cache_mla_large_uneven_sequences). For every request r it
+ * reads the cached-context entries of tokens [start_r, start_r + len_r) out of
+ * a paged cache, through that request's block-table row, and writes them back
+ * to back into a contiguous workspace starting at row min(cu_seq_lens[r], T).
+ * The write is a byte copy, an FP8 E4M3 dequant (section "实现拆解" item 1:
+ * the FP8 -> BF16 upconvert kernel), or a widening cast (the "maybe dequant"
+ * kernel with kv_cache_dtype "auto").
+ *
+ * Conventions for every entry point:
+ *  - Arrays are device memory unless stated otherwise; sizes, strides and
+ *    dtypes are host values. The caller owns every pointer. The library keeps
+ *    no per-call state and allocates no memory.
+ *  - Strides are in ELEMENTS of the array they index; the last (entry)
+ *    dimension has stride 1.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream). Calls are asynchronous on that stream and never synchronise.
+ *  - Host-detected errors return a non-zero pmg_status synchronously; nothing
+ *    is launched and no output is touched.
+ *  - Data errors found on the device (values inside cu_seq_lens, seq_starts or
+ *    block_table) are not host errors: the affected rows are skipped and left
+ *    untouched, a PMG_FLAG_* bit is OR-ed into *error_flag (if non-NULL), and
+ *    the call still returns PMG_OK. The caller reads the flag when it likes.
+ */
+#ifndef PMG_H_
+#define PMG_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element types. PMG_FP8_E4M3 is OCP E4M3 ("fn": bias 7, no infinities,
+ * S.1111.111 is NaN). PMG_U8 is raw bytes. */
+typedef enum pmg_dtype {
+  PMG_BF16 = 0,
+  PMG_FP16 = 1,
+  PMG_FP32 = 2,
+  PMG_FP8_E4M3 = 3,
+  PMG_U8 = 4
+} pmg_dtype;
+
+typedef enum pmg_status {
+  PMG_OK = 0,
+  PMG_ERR_NULL = 1,        /* a required pointer is NULL */
+  PMG_ERR_ARG = 2,         /* a size or stride is out of range */
+  PMG_ERR_DTYPE = 3,       /* unknown dtype or unsupported (src, dst) pair */
+  PMG_ERR_ALIGN = 4,       /* a pointer is not aligned to its element size */
+  PMG_ERR_UNSUPPORTED = 5, /* valid request beyond this build's limits */
+  PMG_ERR_CUDA = 6         /* a CUDA runtime call or the launch failed */
+} pmg_status;
+
+/* Bits OR-ed into *error_flag by the device. */
+#define PMG_FLAG_LOGICAL_BLOCK 1 /* logical block >= block_table_stride: page skipped */
+#define PMG_FLAG_PHYS_BLOCK 2    /* block_table entry outside [0, num_blocks): page skipped */
+#define PMG_FLAG_SEQ_START 4     /* seq_starts[r] < 0 with len_r > 0: request skipped */
+#define PMG_FLAG_CU_ORDER 8      /* cu_seq_lens[0] < 0 or cu decreases: nothing written */
+#define PMG_FLAG_TIMEOUT 16      /* a bounded device wait ran out: output incomplete */
+
+/* Most requests one call accepts (the per-request page plan lives in shared
+ * memory); larger batches return PMG_ERR_UNSUPPORTED. */
+#define PMG_MAX_REQS 4096
+
+/* Options of pmg_gather_ex. */
+#define PMG_OPT_FORCE_SIMT 1u      /* use the SIMT vector kernel even where TMA bulk applies */
+#define PMG_OPT_FORCE_SCALAR 2u    /* use one-element units (the scalar-stride path) */
+#define PMG_OPT_IMPLIED_END 4u     /* cu_seq_lens has num_reqs entries; the last request ends at total_tokens */
+
+/* Data-movement paths (pmg_select_path). */
+typedef enum pmg_path {
+  PMG_PATH_NONE = 0,   /* nothing to do (no rows or no requests): no launch */
+  PMG_PATH_BULK = 1,   /* TMA 1-D bulk copies global -> shared -> global (byte copy, 16-B aligned rows) */
+  PMG_PATH_VECTOR = 2, /* SIMT loads/stores of several elements per thread */
+  PMG_PATH_SCALAR = 3  /* SIMT, one element per access (any alignment) */
+} pmg_path;
+
+/*
+ * pmg_gather — the paged gather (the call of ops.cp_gather_cache in the
+ * section "关键源码片段", with strides, dtypes, scale and stream made explicit).
+ *
+ *  cache               [num_blocks, block_size, >= entry_size] of src_dtype.
+ *  cache_block_stride  elements between consecutive blocks (>= 0).
+ *  cache_token_stride  elements between consecutive slots of a block (>= 0);
+ *                      a value larger than entry_size is a padded row.
+ *  num_blocks          physical blocks; a block id outside [0, num_blocks) is
+ *                      a data error (PMG_FLAG_PHYS_BLOCK).
+ *  block_table         int32 [num_reqs, block_table_stride]: row r maps logical
+ *                      block i of request r (tokens [i*block_size,
+ *                      (i+1)*block_size) of its context) to a physical block.
+ *  cu_seq_lens         int32 [num_reqs + 1]: request r owns output rows
+ *                      [min(cu[r], T), min(cu[r+1], T)); its length is
+ *                      max(min(cu[r+1], T) - min(cu[r], T), 0). Must be
+ *                      non-decreasing from cu[0] >= 0 (else PMG_FLAG_CU_ORDER).
+ *  seq_starts          int32 [num_reqs] or NULL (all zero): the first context
+ *                      token of request r to copy.
+ *  num_reqs            0 <= num_reqs <= PMG_MAX_REQS.
+ *  total_tokens        T >= 0, rows of dst. Rows >= T are never written.
+ *  block_size          tokens per block, >= 1.
+ *  entry_size          elements per token entry, >= 1.
+ *  src_dtype/dst_dtype same dtype: byte copy. PMG_FP8_E4M3 -> PMG_BF16,
+ *                      PMG_FP16 or PMG_FP32: dst = round_to_nearest_even(
+ *                      fp32(x) *fp32 scale). PMG_BF16 or PMG_FP16 -> PMG_FP32:
+ *                      exact widening, no scale. Other pairs: PMG_ERR_DTYPE.
+ *  scale               device fp32 scalar, or NULL for 1.0. Read only when the
+ *                      source is PMG_FP8_E4M3 and the dtypes differ.
+ *  dst                 [>= T, dst_token_stride] of dst_dtype.
+ *  dst_token_stride    elements between output rows, >= entry_size.
+ *  error_flag          device int32 or NULL; PMG_FLAG_* bits are OR-ed in.
+ *  stream              cudaStream_t.
+ * Returns a pmg_status. Only rows of valid pages are written; every other
+ * element of dst (other rows, columns past entry_size) is left as it was.
+ */
+int pmg_gather(const void* cache, int64_t cache_block_stride, int64_t cache_token_stride, int64_t num_blocks,
+               const int32_t* block_table, int64_t block_table_stride, const int32_t* cu_seq_lens,
+               const int32_t* seq_starts, int32_t num_reqs, int64_t total_tokens, int32_t block_size,
+               int32_t entry_size, int32_t src_dtype, int32_t dst_dtype, const float* scale, void* dst,
+               int64_t dst_token_stride, int32_t* error_flag, void* stream);
+
+/*
+ * pmg_gather_ex — pmg_gather with PMG_OPT_* options (0 = pmg_gather).
+ * PMG_OPT_IMPLIED_END selects the page's other calling convention
+ * (map_gather_page_task with has_terminal_start = false, section
+ * "关键源码片段"): cu_seq_lens then holds num_reqs entries and request
+ * num_reqs-1 ends at total_tokens.
+ */
+int pmg_gather_ex(const void* cache, int64_t cache_block_stride, int64_t cache_token_stride, int64_t num_blocks,
+                  const int32_t* block_table, int64_t block_table_stride, const int32_t* cu_seq_lens,
+                  const int32_t* seq_starts, int32_t num_reqs, int64_t total_tokens, int32_t block_size,
+                  int32_t entry_size, int32_t src_dtype, int32_t dst_dtype, const float* scale, void* dst,
+                  int64_t dst_token_stride, int32_t* error_flag, void* stream, uint32_t options);
+
+/*
+ * pmg_select_path — host-only: validates the layout arguments of a gather the
+ * way pmg_gather_ex does and reports the path and the elements moved per
+ * access it would use. Makes no CUDA call. Pointers are only inspected for
+ * alignment and NULL. *path_out receives a pmg_path, *unit_elems_out the
+ * elements per access (0 for PMG_PATH_NONE, 0 for PMG_PATH_BULK).
+ */
+int pmg_select_path(const void* cache, int64_t cache_block_stride, int64_t cache_token_stride,
+                    int64_t num_blocks, const int32_t* block_table, int64_t block_table_stride,
+                    const int32_t* cu_seq_lens, int32_t num_reqs, int64_t total_tokens, int32_t block_size,
+                    int32_t entry_size, int32_t src_dtype, int32_t dst_dtype, const void* dst,
+                    int64_t dst_token_stride, uint32_t options, int32_t* path_out, int32_t* unit_elems_out);
+
+/*
+ * pmg_debug_plan — runs the device page-task mapper alone (section
+ * "实现拆解" item 1 and the GatherPageTask / map_gather_page_task listing:
+ * a flat task id -> (req, logical_block, page_token_begin, page_token_end,
+ * output_token_begin)). Here the mapper is a prefix sum over per-request page
+ * counts plus a binary search, the same device code the gather uses.
+ *  tasks_out      device int32 [max_tasks, 5]: task t is written as
+ *                 {req, logical_block, page_token_begin, page_token_end,
+ *                 output_token_begin} for t < min(num_tasks, max_tasks).
+ *  num_tasks_out  device int64 scalar: the number of tasks.
+ *  error_flag     as in pmg_gather (PMG_FLAG_SEQ_START, PMG_FLAG_CU_ORDER).
+ * A request with len 0 or a negative start has no task; an invalid
+ * cu_seq_lens gives 0 tasks. The block table is not read.
+ */
+int pmg_debug_plan(const int32_t* cu_seq_lens, const int32_t* seq_starts, int32_t num_reqs, int64_t total_tokens,
+                   int32_t block_size, int32_t* tasks_out, int64_t max_tasks, int64_t* num_tasks_out,
+                   int32_t* error_flag, void* stream, uint32_t options);
+
+/* Static description of a status code. Never NULL. */
+const char* pmg_status_string(int status);
+
+/* ABI version of this library: 1. */
+int pmg_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PMG_H_ */

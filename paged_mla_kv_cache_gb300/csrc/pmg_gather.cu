@@ -1,0 +1,1172 @@
+// Paged MLA KV-cache gather for GB300 (sm_103a).
+//
+// What it computes: "MLA cache gather scheduled per logical page"
+// (prhub.com.cn, vllm PR #51739). For each request r, the entries of context
+// tokens [start_r, start_r + len_r) are read through block_table row r out of a
+// paged cache [num_blocks, block_size, entry] and written back to back into
+// dst starting at row min(cu_seq_lens[r], T) (section "关键源码片段": the
+// map_gather_page_task listing fixes the output placement and the page split,
+// the test test_cp_gather_cache_mla_large_uneven_sequences fixes the per-token
+// result). The write is a byte copy, an FP8 E4M3 dequant, or a widening cast
+// (section "实现拆解" item 1: three gather kernels, raw copy, FP8 -> BF16
+// upconvert and maybe-dequant).
+//
+// How this file does it (GB300-first, not the page's kernel):
+//  * Work split. The page gives one CTA per logical page. Here a persistent
+//    grid (a multiple of the SM count) splits the OUTPUT ROWS evenly across
+//    CTAs, so a 300K-token request and a 17-token request cost each CTA the
+//    same bytes; inside its row range a CTA walks page tasks in order.
+//  * Page-task mapper. Every CTA builds, in shared memory, the exclusive prefix
+//    sum of per-request page counts (a block scan over requests). A flat task
+//    id becomes (req, logical_block, page_token_begin, page_token_end,
+//    output_token_begin) by a binary search over that prefix: O(log R) where
+//    the page's mapper scans all requests linearly.
+//  * Broadcast. The tasks of a CTA's range are resolved in parallel (one
+//    thread per task: map, one block-table read, bounds checks) into a
+//    shared-memory segment table that the whole CTA then reads.
+//  * Movement. Byte copies of 16-byte aligned rows use TMA 1-D bulk copies
+//    (cp.async.bulk global -> shared with an mbarrier, then shared -> global
+//    bulk stores), a multi-stage ring per CTA driven by one thread. Converts and
+//    unaligned layouts use SIMT loads and stores of 16, 8, 4, 2 or 1 bytes per
+//    access with the convert done in registers.
+//  * Safety. 64-bit byte offsets everywhere; the logical block is checked
+//    against block_table_stride and the physical id against num_blocks in
+//    every path (the review section "评论区精华" reports both checks missing
+//    and an int32 overflow of output_token_begin * entry_bytes). Bad pages are
+//    skipped and reported in an error flag; nothing traps, and every wait on
+//    an mbarrier is bounded in time.
+//  * No tensor cores: the path is pure data movement, bound by HBM.
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <algorithm>
+#include <cstdlib>
+#include <mutex>
+
+#include "pmg.h"
+
+namespace {
+
+constexpr int kPlanThreads = 256;        // SIMT kernel / debug-plan CTA size
+constexpr int kBulkThreads = 128;        // bulk kernel CTA size
+constexpr int kBulkStages = 4;           // TMA ring depth per CTA
+constexpr int kMaxStageBytes = 48 * 1024;
+constexpr int kUnroll = 4;               // SIMT units in flight per thread
+constexpr int kMinRowsPerCta = 8;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per bounded wait
+
+enum Conv : int {
+  CONV_COPY = 0,
+  CONV_E4M3_BF16 = 1,
+  CONV_E4M3_F16 = 2,
+  CONV_E4M3_F32 = 3,
+  CONV_BF16_F32 = 4,
+  CONV_F16_F32 = 5,
+};
+
+struct Params {
+  const uint8_t* cache;
+  int64_t blk_stride_b;   // bytes between blocks
+  int64_t tok_stride_b;   // bytes between slots
+  int64_t num_blocks;
+  const int32_t* bt;
+  int64_t bt_stride;      // elements
+  const int32_t* cu;
+  const int32_t* ss;      // may be null
+  int32_t R;
+  int32_t T;              // total_tokens clamped to INT32_MAX
+  int32_t B;
+  int32_t implied_end;    // cu has R entries; the last request ends at T
+  int32_t row_src_bytes;  // entry_size * src element bytes
+  int32_t row_dst_bytes;  // entry_size * dst element bytes
+  uint8_t* dst;
+  int64_t dst_stride_b;   // bytes between output rows
+  const float* scale;     // may be null
+  int32_t* err;           // may be null
+  // SIMT mover
+  int32_t units_per_row;  // entry_size / elements per unit
+  uint32_t upr_magic;     // fast division by units_per_row (fast_div)
+  int32_t upr_shift;
+  int32_t dense;          // src and dst rows are back to back: no row split
+  // bulk mover
+  int32_t stage_bytes;    // bytes of one ring stage
+  int32_t rows_per_stage;
+  int32_t src_dense;
+  int32_t dst_dense;
+};
+
+// ---------------------------------------------------------------------------
+// Small device helpers
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void set_flag(const Params& p, int bits) {
+  if (bits != 0 && p.err != nullptr) atomicOr(p.err, bits);
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// first index i in [0, n) with a[i] > key, or n (a is non-decreasing)
+__device__ __forceinline__ int upper_bound_i32(const int32_t* a, int n, int64_t key) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (static_cast<int64_t>(a[mid]) <= key) lo = mid + 1; else hi = mid;
+  }
+  return lo;
+}
+
+// Division of a 32-bit unsigned n by a fixed d >= 1 with one multiply-high,
+// an add and a shift: with l = ceil(log2 d) and m = floor(2^32 (2^l - d) / d) + 1,
+// floor(n / d) = (mulhi(m, n) + n) >> l for every 32-bit n (the invariant-
+// divisor method of Granlund and Montgomery, 1994). The host computes m and l.
+__device__ __forceinline__ uint32_t fast_div(uint32_t n, uint32_t magic, int shift) {
+  const uint64_t hi = __umulhi(magic, n);
+  return static_cast<uint32_t>((hi + n) >> shift);
+}
+
+// ---------------------------------------------------------------------------
+// Page plan: per-request output begins, starts and the page-count prefix
+// ---------------------------------------------------------------------------
+
+struct PlanView {
+  int32_t* ob;  // [R + 1] clamped output begins; ob[R] = end of the last request
+  int32_t* st;  // [R] source starts
+  int32_t* P;   // [R + 1] exclusive prefix of page counts
+};
+
+__device__ __forceinline__ PlanView plan_view(uint8_t* base, int R) {
+  PlanView v;
+  v.ob = reinterpret_cast<int32_t*>(base);
+  v.st = v.ob + (R + 1);
+  v.P = v.st + R;
+  return v;
+}
+
+// Pages of request r: the logical blocks its source range [s, s + len) touches
+// (0 for len == 0 or a negative start).
+__device__ __forceinline__ int32_t request_pages(const PlanView& v, int r, int B) {
+  const int64_t len = static_cast<int64_t>(v.ob[r + 1]) - v.ob[r];
+  const int64_t s = v.st[r];
+  if (len <= 0 || s < 0) return 0;
+  const int64_t first = s / B;
+  const int64_t last_excl = (s + len + B - 1) / B;
+  return static_cast<int32_t>(last_excl - first);
+}
+
+// Builds the plan with all threads of the CTA. Returns the number of page
+// tasks, or -1 when cu_seq_lens is not non-decreasing from a non-negative
+// start (then nothing may be written). report_flags: this CTA reports the
+// plan-level flag bits (one CTA per launch does, to keep atomics rare).
+__device__ int build_plan(const Params& p, const PlanView& v, bool report_flags) {
+  __shared__ int32_t warp_sums[32];
+  __shared__ int32_t total_pages;
+  const int tid = threadIdx.x;
+  const int nt = blockDim.x;
+  const int R = p.R;
+  const int64_t T = p.T;
+
+  int bad = 0;
+  int bad_start = 0;
+  for (int r = tid; r <= R; r += nt) {
+    int64_t c;
+    if (p.implied_end && r == R) {
+      const int64_t prev = R > 0 ? static_cast<int64_t>(__ldg(p.cu + R - 1)) : 0;
+      c = prev > T ? prev : T;
+    } else {
+      c = __ldg(p.cu + r);
+    }
+    if (r == 0 && c < 0) bad = 1;
+    if (r > 0) {
+      const int64_t prev = __ldg(p.cu + r - 1);
+      if (c < prev) bad = 1;
+    }
+    v.ob[r] = static_cast<int32_t>(c < T ? c : T);
+    if (r < R) v.st[r] = p.ss ? __ldg(p.ss + r) : 0;
+  }
+  if (__syncthreads_or(bad)) {
+    if (report_flags && tid == 0) set_flag(p, PMG_FLAG_CU_ORDER);
+    return -1;
+  }
+
+  // exclusive scan of page counts: each thread owns a contiguous run of requests
+  const int per = (R + nt - 1) / nt;
+  const int rb = min(tid * per, R);
+  const int re = min(rb + per, R);
+  int32_t local = 0;
+  for (int r = rb; r < re; ++r) {
+    local += request_pages(v, r, p.B);
+    if (v.st[r] < 0 && v.ob[r + 1] > v.ob[r]) bad_start = 1;
+  }
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const int nwarps = (nt + 31) >> 5;
+  int32_t x = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_sums[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int32_t w = lane < nwarps ? warp_sums[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < nwarps) warp_sums[lane] = w;
+    if (lane == nwarps - 1) total_pages = w;
+  }
+  __syncthreads();
+  int32_t base = (warp > 0 ? warp_sums[warp - 1] : 0) + x - local;
+  for (int r = rb; r < re; ++r) {
+    v.P[r] = base;
+    base += request_pages(v, r, p.B);
+  }
+  if (tid == 0) v.P[R] = total_pages;
+  if (__syncthreads_or(bad_start) && report_flags && tid == 0) set_flag(p, PMG_FLAG_SEQ_START);
+  return total_pages;
+}
+
+struct PageTask {
+  int32_t req;
+  int64_t logical_block;
+  int32_t begin;  // page_token_begin (relative to the page start)
+  int32_t end;    // page_token_end (exclusive)
+  int32_t out;    // output_token_begin
+};
+
+// Flat task id -> page task: binary search over the page-count prefix, then
+// the page's clipping of [start, start + len) to logical block lb.
+__device__ __forceinline__ PageTask map_task(const PlanView& v, int R, int B, int32_t t) {
+  const int r = upper_bound_i32(v.P, R + 1, t) - 1;
+  const int64_t j = static_cast<int64_t>(t) - v.P[r];
+  const int64_t s = v.st[r];
+  const int64_t len = static_cast<int64_t>(v.ob[r + 1]) - v.ob[r];
+  const int64_t lb = s / B + j;
+  const int64_t page_begin = lb * B;
+  const int64_t cb = s > page_begin ? s : page_begin;
+  const int64_t ce = (s + len) < (page_begin + B) ? (s + len) : (page_begin + B);
+  PageTask k;
+  k.req = r;
+  k.logical_block = lb;
+  k.begin = static_cast<int32_t>(cb - page_begin);
+  k.end = static_cast<int32_t>(ce - page_begin);
+  k.out = static_cast<int32_t>(v.ob[r] + (cb - s));
+  return k;
+}
+
+// The CTA's share of output rows [row0, row1) and its first task id.
+struct CtaRange {
+  int32_t row0, row1, t0;
+};
+
+__device__ __forceinline__ CtaRange cta_range(const PlanView& v, int R, int B, int32_t num_tasks) {
+  CtaRange c;
+  const int64_t lo = v.ob[0];
+  const int64_t hi = v.ob[R];
+  const int64_t rows = hi - lo;
+  c.row0 = static_cast<int32_t>(lo + rows * blockIdx.x / gridDim.x);
+  c.row1 = static_cast<int32_t>(lo + rows * (blockIdx.x + 1) / gridDim.x);
+  c.t0 = num_tasks;
+  if (c.row0 >= c.row1 || num_tasks <= 0) return c;
+  // request containing row0: last r with ob[r] <= row0 (it is non-empty)
+  const int r = upper_bound_i32(v.ob, R + 1, c.row0) - 1;
+  const int64_t s = v.st[r];
+  if (s < 0) {
+    c.t0 = v.P[r];  // no task in r; start with the next request's tasks
+  } else {
+    const int64_t pos = s + (c.row0 - v.ob[r]);
+    c.t0 = v.P[r] + static_cast<int32_t>(pos / B - s / B);
+  }
+  return c;
+}
+
+// A clipped, bounds-checked page task: rows [dst_row0, dst_row0 + nrows) of
+// dst come from consecutive slots of one physical block.
+struct Segment {
+  int64_t src;     // byte offset into the cache
+  int64_t dst;     // byte offset into dst
+  int32_t nrows;   // 0 = nothing to copy
+  int32_t pad;
+};
+
+// Resolves task t for a CTA owning rows [row0, row1). Returns false when the
+// task starts at or past row1 (tasks are ordered by output row, so every
+// later task does too).
+__device__ __forceinline__ bool resolve_segment(const Params& p, const PlanView& v, int32_t t, int32_t num_tasks,
+                                                int32_t row0, int32_t row1, Segment& seg) {
+  seg.nrows = 0;
+  seg.src = 0;
+  seg.dst = 0;
+  if (t >= num_tasks) return false;
+  const PageTask k = map_task(v, p.R, p.B, t);
+  if (k.out >= row1) return false;
+  const int64_t lo = k.out > row0 ? k.out : row0;
+  const int64_t task_end = static_cast<int64_t>(k.out) + (k.end - k.begin);
+  const int64_t hi = task_end < row1 ? task_end : row1;
+  if (hi <= lo) return true;
+  if (k.logical_block >= p.bt_stride) {
+    set_flag(p, PMG_FLAG_LOGICAL_BLOCK);
+    return true;
+  }
+  const int64_t phys = __ldg(p.bt + static_cast<int64_t>(k.req) * p.bt_stride + k.logical_block);
+  if (phys < 0 || phys >= p.num_blocks) {
+    set_flag(p, PMG_FLAG_PHYS_BLOCK);
+    return true;
+  }
+  const int64_t slot = k.begin + (lo - k.out);
+  seg.src = phys * p.blk_stride_b + slot * p.tok_stride_b;
+  seg.dst = lo * p.dst_stride_b;
+  seg.nrows = static_cast<int32_t>(hi - lo);
+  return true;
+}
+
+// ---------------------------------------------------------------------------
+// TMA bulk path (byte copy, 16-byte aligned rows)
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for the given phase parity; gives up after kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  uint32_t spins = 0;
+  while (!mbar_try_wait(bar, parity)) {
+    if ((++spins & 255u) == 0 && global_ns() - t0 > kWaitLimitNs) return false;
+  }
+  return true;
+}
+
+__device__ __forceinline__ uint64_t evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar,
+                                          uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+      ::"r"(smem_addr(smem_dst)), "l"(gsrc), "r"(bytes), "r"(smem_addr(bar)), "l"(pol)
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_store(void* gdst, const void* smem_src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(smem_addr(smem_src)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Wait until at most n committed bulk-store groups still read shared memory.
+__device__ __forceinline__ void bulk_wait_read_upto(int n) {
+  static_assert(kBulkStages == 4, "update the cases below");
+  switch (n) {
+    case 0: asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); break;
+    case 1: asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); break;
+    case 2: asm volatile("cp.async.bulk.wait_group.read 2;" ::: "memory"); break;
+    default: asm volatile("cp.async.bulk.wait_group.read 3;" ::: "memory"); break;
+  }
+}
+
+struct Chunk {
+  int64_t src;
+  int64_t dst;
+  int32_t nrows;
+};
+
+// Walks the segment table chunk by chunk (at most rows_per_stage rows each).
+struct ChunkIter {
+  int seg;
+  int32_t row;
+  __device__ __forceinline__ bool next(const Segment* segs, int nseg, int32_t rows_per_stage, const Params& p,
+                                       Chunk& c) {
+    while (seg < nseg && row >= segs[seg].nrows) {
+      ++seg;
+      row = 0;
+    }
+    if (seg >= nseg) return false;
+    const Segment& s = segs[seg];
+    const int32_t n = min(rows_per_stage, s.nrows - row);
+    c.src = s.src + static_cast<int64_t>(row) * p.tok_stride_b;
+    c.dst = s.dst + static_cast<int64_t>(row) * p.dst_stride_b;
+    c.nrows = n;
+    row += n;
+    return true;
+  }
+};
+
+__global__ void __launch_bounds__(kBulkThreads) gather_bulk_kernel(const __grid_constant__ Params p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t full_bar[kBulkStages];
+  __shared__ Chunk stage_chunk[kBulkStages];
+  __shared__ Segment segs[kBulkThreads];
+  __shared__ int abort_flag;
+
+  // layout: [stages][plan]; stage buffers first keeps them 128-byte aligned
+  uint8_t* stage_base = smem;
+  const PlanView v = plan_view(smem + static_cast<size_t>(kBulkStages) * p.stage_bytes, p.R);
+
+  const int32_t num_tasks = build_plan(p, v, blockIdx.x == 0);
+  if (num_tasks <= 0) return;
+  const CtaRange range = cta_range(v, p.R, p.B, num_tasks);
+  if (range.row0 >= range.row1) return;
+
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    for (int s = 0; s < kBulkStages; ++s) mbar_init(&full_bar[s], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    abort_flag = 0;
+  }
+  __syncthreads();
+
+  const uint64_t pol = evict_first_policy();
+  const uint32_t row_bytes = static_cast<uint32_t>(p.row_src_bytes);
+  uint32_t loads = 0, stores = 0;  // chunks loaded / stored so far (tid 0 only)
+
+  for (int32_t tb = range.t0;; tb += kBulkThreads) {
+    Segment seg;
+    const bool active = resolve_segment(p, v, tb + tid, num_tasks, range.row0, range.row1, seg);
+    segs[tid] = seg;
+    const int nseg = __syncthreads_count(active);
+    if (tid == 0 && nseg > 0) {
+      ChunkIter li{0, 0};
+      bool more = true;
+      bool ok = true;
+      while (ok) {
+        // keep up to kBulkStages chunks loading ahead of the stores
+        while (more && loads - stores < static_cast<uint32_t>(kBulkStages)) {
+          Chunk c;
+          more = li.next(segs, nseg, p.rows_per_stage, p, c);
+          if (!more) break;
+          const int s = static_cast<int>(loads % kBulkStages);
+          if (loads >= static_cast<uint32_t>(kBulkStages)) {
+            // the store that last used stage s must have finished reading it
+            bulk_wait_read_upto(static_cast<int>(stores - 1 - (loads - kBulkStages)));
+          }
+          stage_chunk[s] = c;
+          uint8_t* buf = stage_base + static_cast<size_t>(s) * p.stage_bytes;
+          const uint32_t bytes = static_cast<uint32_t>(c.nrows) * row_bytes;
+          mbar_arrive_expect_tx(&full_bar[s], bytes);
+          if (p.src_dense) {
+            bulk_load(buf, p.cache + c.src, bytes, &full_bar[s], pol);
+          } else {
+            for (int32_t i = 0; i < c.nrows; ++i)
+              bulk_load(buf + static_cast<size_t>(i) * row_bytes, p.cache + c.src + i * p.tok_stride_b, row_bytes,
+                        &full_bar[s], pol);
+          }
+          ++loads;
+        }
+        if (stores == loads) break;
+        const int s = static_cast<int>(stores % kBulkStages);
+        if (!mbar_wait_bounded(&full_bar[s], (stores / kBulkStages) & 1u)) {
+          ok = false;
+          break;
+        }
+        const Chunk c = stage_chunk[s];
+        const uint8_t* buf = stage_base + static_cast<size_t>(s) * p.stage_bytes;
+        if (p.dst_dense) {
+          bulk_store(p.dst + c.dst, buf, static_cast<uint32_t>(c.nrows) * row_bytes);
+        } else {
+          for (int32_t i = 0; i < c.nrows; ++i)
+            bulk_store(p.dst + c.dst + i * p.dst_stride_b, buf + static_cast<size_t>(i) * row_bytes, row_bytes);
+        }
+        bulk_commit();
+        ++stores;
+      }
+      if (!ok) {
+        // a load never completed: report, give the other loads in flight a
+        // bounded chance to land, then stop this CTA
+        set_flag(p, PMG_FLAG_TIMEOUT);
+        for (uint32_t k = stores + 1; k < loads; ++k)
+          (void)mbar_wait_bounded(&full_bar[k % kBulkStages], (k / kBulkStages) & 1u);
+        abort_flag = 1;
+      }
+    }
+    const bool last = nseg < kBulkThreads;
+    __syncthreads();
+    if (last || abort_flag) break;
+  }
+  if (tid == 0) bulk_wait_all();
+}
+
+// ---------------------------------------------------------------------------
+// SIMT path: converts and layouts the bulk path does not take
+// ---------------------------------------------------------------------------
+
+// Raw storage of one access: BYTES bytes in whole 32-bit words (or a sub-word).
+template <int BYTES>
+struct Raw {
+  static constexpr int kWords = BYTES >= 4 ? BYTES / 4 : 1;
+  uint32_t w[kWords];
+};
+
+template <int BYTES>
+__device__ __forceinline__ void load_raw(const uint8_t* src, Raw<BYTES>& r) {
+  if constexpr (BYTES == 16) {
+    const uint4 x = __ldcs(reinterpret_cast<const uint4*>(src));
+    r.w[0] = x.x; r.w[1] = x.y; r.w[2] = x.z; r.w[3] = x.w;
+  } else if constexpr (BYTES == 8) {
+    const uint2 x = __ldcs(reinterpret_cast<const uint2*>(src));
+    r.w[0] = x.x; r.w[1] = x.y;
+  } else if constexpr (BYTES == 4) {
+    r.w[0] = __ldcs(reinterpret_cast<const unsigned int*>(src));
+  } else if constexpr (BYTES == 2) {
+    r.w[0] = __ldcs(reinterpret_cast<const unsigned short*>(src));
+  } else {
+    static_assert(BYTES == 1, "unit size");
+    r.w[0] = __ldcs(reinterpret_cast<const unsigned char*>(src));
+  }
+}
+
+template <int BYTES>
+__device__ __forceinline__ void store_raw(uint8_t* dst, const Raw<BYTES>& r) {
+  if constexpr (BYTES >= 16) {
+#pragma unroll
+    for (int i = 0; i < BYTES / 16; ++i)
+      *reinterpret_cast<uint4*>(dst + 16 * i) = make_uint4(r.w[4 * i], r.w[4 * i + 1], r.w[4 * i + 2], r.w[4 * i + 3]);
+  } else if constexpr (BYTES == 8) {
+    *reinterpret_cast<uint2*>(dst) = make_uint2(r.w[0], r.w[1]);
+  } else if constexpr (BYTES == 4) {
+    *reinterpret_cast<uint32_t*>(dst) = r.w[0];
+  } else if constexpr (BYTES == 2) {
+    *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(r.w[0]);
+  } else {
+    static_assert(BYTES == 1, "unit size");
+    *dst = static_cast<uint8_t>(r.w[0]);
+  }
+}
+
+template <int CONV>
+struct ConvTraits;
+template <> struct ConvTraits<CONV_COPY> { static constexpr int es = 1, ed = 1; };
+template <> struct ConvTraits<CONV_E4M3_BF16> { static constexpr int es = 1, ed = 2; };
+template <> struct ConvTraits<CONV_E4M3_F16> { static constexpr int es = 1, ed = 2; };
+template <> struct ConvTraits<CONV_E4M3_F32> { static constexpr int es = 1, ed = 4; };
+template <> struct ConvTraits<CONV_BF16_F32> { static constexpr int es = 2, ed = 4; };
+template <> struct ConvTraits<CONV_F16_F32> { static constexpr int es = 2, ed = 4; };
+
+// two e4m3 codes (low 16 bits of `pair`) -> two exact fp32 values
+__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t pair) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(pair & 0xFFFFu), __NV_E4M3);
+  __half2 hh;
+  hh = h;
+  return __half22float2(hh);
+}
+
+__device__ __forceinline__ uint32_t pack_out2(float a, float b, int conv) {
+  if (conv == CONV_E4M3_BF16) {
+    const __nv_bfloat162 o = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&o);
+  } else {
+    const __half2 o = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&o);
+  }
+}
+
+// Converts N elements held in `in` into `out`.
+template <int CONV, int N>
+__device__ __forceinline__ void convert_unit(const Raw<N * ConvTraits<CONV>::es>& in,
+                                             Raw<N * ConvTraits<CONV>::ed>& out, float scale) {
+  if constexpr (CONV == CONV_COPY) {
+#pragma unroll
+    for (int i = 0; i < Raw<N>::kWords; ++i) out.w[i] = in.w[i];
+  } else if constexpr (CONV == CONV_E4M3_BF16 || CONV == CONV_E4M3_F16 || CONV == CONV_E4M3_F32) {
+    if constexpr (N == 1) {
+      const float2 f = e4m3x2_to_f32x2(in.w[0]);
+      const float y = __fmul_rn(f.x, scale);
+      if constexpr (CONV == CONV_E4M3_F32) {
+        out.w[0] = __float_as_uint(y);
+      } else if constexpr (CONV == CONV_E4M3_BF16) {
+        out.w[0] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
+      } else {
+        out.w[0] = __half_as_ushort(__float2half_rn(y));
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < N / 4; ++i) {
+        const uint32_t w = in.w[i];
+        const float2 lo = e4m3x2_to_f32x2(w);
+        const float2 hi = e4m3x2_to_f32x2(w >> 16);
+        const float a = __fmul_rn(lo.x, scale), b = __fmul_rn(lo.y, scale);
+        const float c = __fmul_rn(hi.x, scale), d = __fmul_rn(hi.y, scale);
+        if constexpr (CONV == CONV_E4M3_F32) {
+          out.w[4 * i + 0] = __float_as_uint(a);
+          out.w[4 * i + 1] = __float_as_uint(b);
+          out.w[4 * i + 2] = __float_as_uint(c);
+          out.w[4 * i + 3] = __float_as_uint(d);
+        } else {
+          out.w[2 * i + 0] = pack_out2(a, b, CONV);
+          out.w[2 * i + 1] = pack_out2(c, d, CONV);
+        }
+      }
+    }
+  } else {
+    // bf16 / fp16 -> fp32, exact
+    if constexpr (N == 1) {
+      const uint32_t h = in.w[0] & 0xFFFFu;
+      if constexpr (CONV == CONV_BF16_F32) {
+        out.w[0] = h << 16;
+      } else {
+        out.w[0] = __float_as_uint(__half2float(__ushort_as_half(static_cast<unsigned short>(h))));
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < N / 2; ++i) {
+        const uint32_t w = in.w[i];
+        if constexpr (CONV == CONV_BF16_F32) {
+          out.w[2 * i + 0] = w << 16;
+          out.w[2 * i + 1] = w & 0xFFFF0000u;
+        } else {
+          out.w[2 * i + 0] = __float_as_uint(__half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xFFFFu))));
+          out.w[2 * i + 1] = __float_as_uint(__half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16))));
+        }
+      }
+    }
+  }
+}
+
+template <int CONV, int N>
+__global__ void __launch_bounds__(kPlanThreads) gather_simt_kernel(const __grid_constant__ Params p) {
+  constexpr int kInBytes = N * ConvTraits<CONV>::es;
+  constexpr int kOutBytes = N * ConvTraits<CONV>::ed;
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ Segment segs[kPlanThreads];
+  __shared__ int64_t unit_prefix[kPlanThreads + 1];
+  __shared__ int64_t warp_units[kPlanThreads / 32];
+
+  const PlanView v = plan_view(smem, p.R);
+  const int32_t num_tasks = build_plan(p, v, blockIdx.x == 0);
+  if (num_tasks <= 0) return;
+  const CtaRange range = cta_range(v, p.R, p.B, num_tasks);
+  if (range.row0 >= range.row1) return;
+
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  float scale = 1.0f;
+  if (CONV == CONV_E4M3_BF16 || CONV == CONV_E4M3_F16 || CONV == CONV_E4M3_F32) {
+    if (p.scale != nullptr) scale = __ldg(p.scale);
+  }
+  const uint32_t upr = static_cast<uint32_t>(p.units_per_row);
+
+  for (int32_t tb = range.t0;; tb += kPlanThreads) {
+    Segment seg;
+    const bool active = resolve_segment(p, v, tb + tid, num_tasks, range.row0, range.row1, seg);
+    segs[tid] = seg;
+    // exclusive scan of units per segment
+    const int64_t my_units = static_cast<int64_t>(seg.nrows) * upr;
+    int64_t x = my_units;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_units[warp] = x;
+    const int nseg = __syncthreads_count(active);
+    if (warp == 0) {
+      int64_t w = lane < kPlanThreads / 32 ? warp_units[lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int64_t y = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += y;
+      }
+      if (lane < kPlanThreads / 32) warp_units[lane] = w;
+    }
+    __syncthreads();
+    unit_prefix[tid] = (warp > 0 ? warp_units[warp - 1] : 0) + x - my_units;
+    if (tid == 0) unit_prefix[kPlanThreads] = warp_units[kPlanThreads / 32 - 1];
+    __syncthreads();
+
+    const int64_t total = unit_prefix[kPlanThreads];
+    int cur = 0;
+    for (int64_t g0 = tid; g0 < total; g0 += static_cast<int64_t>(kUnroll) * kPlanThreads) {
+      Raw<kInBytes> in[kUnroll];
+      uint8_t* dptr[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int64_t g = g0 + static_cast<int64_t>(u) * kPlanThreads;
+        dptr[u] = nullptr;
+        if (g < total) {
+          while (unit_prefix[cur + 1] <= g) ++cur;
+          const Segment& s = segs[cur];
+          const int64_t local = g - unit_prefix[cur];
+          int64_t so, dof;
+          if (p.dense) {
+            so = s.src + local * kInBytes;
+            dof = s.dst + local * kOutBytes;
+          } else {
+            const uint32_t row = fast_div(static_cast<uint32_t>(local), p.upr_magic, p.upr_shift);
+            const uint32_t col = static_cast<uint32_t>(local) - row * upr;
+            so = s.src + static_cast<int64_t>(row) * p.tok_stride_b + static_cast<int64_t>(col) * kInBytes;
+            dof = s.dst + static_cast<int64_t>(row) * p.dst_stride_b + static_cast<int64_t>(col) * kOutBytes;
+          }
+          load_raw<kInBytes>(p.cache + so, in[u]);
+          dptr[u] = p.dst + dof;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        if (dptr[u] != nullptr) {
+          Raw<kOutBytes> out;
+          convert_unit<CONV, N>(in[u], out, scale);
+          store_raw<kOutBytes>(dptr[u], out);
+        }
+      }
+    }
+    const bool last = nseg < kPlanThreads;
+    __syncthreads();
+    if (last) break;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Debug plan: the mapper alone
+// ---------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(kPlanThreads) debug_plan_kernel(const __grid_constant__ Params p, int32_t* tasks_out,
+                                                                  int64_t max_tasks, int64_t* num_tasks_out) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const PlanView v = plan_view(smem, p.R);
+  const int32_t n = build_plan(p, v, true);
+  const int32_t num = n < 0 ? 0 : n;
+  if (threadIdx.x == 0) *num_tasks_out = num;
+  const int64_t lim = num < max_tasks ? num : max_tasks;
+  for (int64_t t = threadIdx.x; t < lim; t += blockDim.x) {
+    const PageTask k = map_task(v, p.R, p.B, static_cast<int32_t>(t));
+    int32_t* o = tasks_out + t * 5;
+    o[0] = k.req;
+    o[1] = static_cast<int32_t>(k.logical_block);
+    o[2] = k.begin;
+    o[3] = k.end;
+    o[4] = k.out;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+
+int elem_bytes(int dt) {
+  switch (dt) {
+    case PMG_BF16: return 2;
+    case PMG_FP16: return 2;
+    case PMG_FP32: return 4;
+    case PMG_FP8_E4M3: return 1;
+    case PMG_U8: return 1;
+    default: return 0;
+  }
+}
+
+// -1 for an unsupported pair
+int conv_of(int src, int dst) {
+  if (elem_bytes(src) == 0 || elem_bytes(dst) == 0) return -1;
+  if (src == dst) return CONV_COPY;
+  if (src == PMG_FP8_E4M3) {
+    if (dst == PMG_BF16) return CONV_E4M3_BF16;
+    if (dst == PMG_FP16) return CONV_E4M3_F16;
+    if (dst == PMG_FP32) return CONV_E4M3_F32;
+  }
+  if (dst == PMG_FP32) {
+    if (src == PMG_BF16) return CONV_BF16_F32;
+    if (src == PMG_FP16) return CONV_F16_F32;
+  }
+  return -1;
+}
+
+// Target bytes of one TMA ring stage. PMG_BULK_STAGE_KB (8..48) overrides the
+// default for tuning sweeps; it changes only the chunking, never the result.
+int bulk_stage_target_bytes() {
+  static const int v = [] {
+    const char* e = std::getenv("PMG_BULK_STAGE_KB");
+    int kb = e ? std::atoi(e) : 24;
+    if (kb < 8) kb = 8;
+    if (kb > kMaxStageBytes / 1024) kb = kMaxStageBytes / 1024;
+    return kb * 1024;
+  }();
+  return v;
+}
+
+bool aligned(const void* ptr, int64_t a) { return (reinterpret_cast<uintptr_t>(ptr) % static_cast<uint64_t>(a)) == 0; }
+
+struct Plan {
+  int path;         // pmg_path
+  int conv;
+  int unit;         // elements per access for SIMT (bytes for CONV_COPY)
+  Params prm;
+};
+
+// candidate units (elements per access; bytes for a byte copy)
+int unit_candidates(int conv, int* out) {
+  switch (conv) {
+    case CONV_COPY: out[0] = 16; out[1] = 8; out[2] = 4; out[3] = 2; out[4] = 1; return 5;
+    case CONV_E4M3_BF16:
+    case CONV_E4M3_F16:
+    case CONV_E4M3_F32: out[0] = 16; out[1] = 4; out[2] = 1; return 3;
+    default: out[0] = 8; out[1] = 2; out[2] = 1; return 3;
+  }
+}
+
+// Validation and path choice: the host half of every entry point. No CUDA call.
+int make_plan(const void* cache, int64_t cbs, int64_t cts, int64_t num_blocks, const int32_t* bt, int64_t bt_stride,
+              const int32_t* cu, const int32_t* ss, int32_t R, int64_t T, int32_t B, int32_t E, int32_t sdt,
+              int32_t ddt, const float* scale, const void* dst, int64_t dts, int32_t* err, uint32_t options,
+              Plan& out) {
+  out.path = PMG_PATH_NONE;
+  out.unit = 0;
+  const int conv = conv_of(sdt, ddt);
+  if (conv < 0) return PMG_ERR_DTYPE;
+  if (R < 0 || T < 0 || B < 1 || E < 1 || num_blocks < 0 || bt_stride < 0 || cbs < 0 || cts < 0 || dts < E)
+    return PMG_ERR_ARG;
+  if (options & ~(PMG_OPT_FORCE_SIMT | PMG_OPT_FORCE_SCALAR | PMG_OPT_IMPLIED_END)) return PMG_ERR_ARG;
+  if (R > PMG_MAX_REQS) return PMG_ERR_UNSUPPORTED;
+  const int es = elem_bytes(sdt), ed = elem_bytes(ddt);
+  if (static_cast<int64_t>(E) * ed > INT32_MAX || static_cast<int64_t>(E) * es > INT32_MAX) return PMG_ERR_UNSUPPORTED;
+  if (R == 0 || T == 0) {
+    out.conv = conv;
+    return PMG_OK;  // nothing to write: no launch
+  }
+  if (cache == nullptr || bt == nullptr || cu == nullptr || dst == nullptr) return PMG_ERR_NULL;
+  if (!aligned(cache, es) || !aligned(dst, ed) || !aligned(bt, 4) || !aligned(cu, 4) ||
+      (ss != nullptr && !aligned(ss, 4)) || (scale != nullptr && !aligned(scale, 4)) ||
+      (err != nullptr && !aligned(err, 4)))
+    return PMG_ERR_ALIGN;
+  // strides in bytes must not overflow int64
+  if (cbs > INT64_MAX / es / 2 || cts > INT64_MAX / es / 2 || dts > INT64_MAX / ed / 2) return PMG_ERR_ARG;
+
+  Params& q = out.prm;
+  q = Params{};
+  q.cache = static_cast<const uint8_t*>(cache);
+  q.blk_stride_b = cbs * es;
+  q.tok_stride_b = cts * es;
+  q.num_blocks = num_blocks;
+  q.bt = bt;
+  q.bt_stride = bt_stride;
+  q.cu = cu;
+  q.ss = ss;
+  q.R = R;
+  q.T = static_cast<int32_t>(T < INT32_MAX ? T : INT32_MAX);
+  q.B = B;
+  q.implied_end = (options & PMG_OPT_IMPLIED_END) ? 1 : 0;
+  q.row_src_bytes = E * es;
+  q.row_dst_bytes = E * ed;
+  q.dst = static_cast<uint8_t*>(const_cast<void*>(dst));
+  q.dst_stride_b = dts * ed;
+  q.scale = scale;
+  q.err = err;
+  out.conv = conv;
+
+  // largest access unit every row start and row length allows
+  int cand[5];
+  const int ncand = unit_candidates(conv, cand);
+  int unit = 1;
+  for (int i = 0; i < ncand; ++i) {
+    const int n = cand[i];
+    // for a byte copy the unit counts bytes of the row
+    const int64_t row_units_base = (conv == CONV_COPY) ? static_cast<int64_t>(E) * es : E;
+    const int64_t in_b = (conv == CONV_COPY) ? n : static_cast<int64_t>(n) * es;
+    const int64_t out_b = (conv == CONV_COPY) ? n : static_cast<int64_t>(n) * ed;
+    const int64_t out_align = out_b > 16 ? 16 : out_b;
+    if (row_units_base % n != 0) continue;
+    if (!aligned(cache, in_b) || q.blk_stride_b % in_b != 0 || q.tok_stride_b % in_b != 0) continue;
+    if (!aligned(dst, out_align) || q.dst_stride_b % out_align != 0) continue;
+    unit = n;
+    break;
+  }
+  if (options & PMG_OPT_FORCE_SCALAR) unit = (conv == CONV_COPY) ? es : 1;
+  out.unit = unit;
+
+  const bool bulk_ok = conv == CONV_COPY && unit == 16 && q.row_src_bytes <= kMaxStageBytes &&
+                       !(options & (PMG_OPT_FORCE_SIMT | PMG_OPT_FORCE_SCALAR));
+  if (bulk_ok) {
+    out.path = PMG_PATH_BULK;
+    q.src_dense = q.tok_stride_b == q.row_src_bytes;
+    q.dst_dense = q.dst_stride_b == q.row_dst_bytes;
+    // ring stages of whole rows, about 32 KB each
+    const int32_t rows = std::max(1, bulk_stage_target_bytes() / q.row_src_bytes);
+    q.rows_per_stage = rows;
+    q.stage_bytes = rows * q.row_src_bytes;
+    out.unit = 0;
+  } else {
+    const int64_t unit_elems = (conv == CONV_COPY) ? unit / es : unit;
+    out.path = (unit_elems > 1) ? PMG_PATH_VECTOR : PMG_PATH_SCALAR;
+    const int64_t upr = (conv == CONV_COPY) ? static_cast<int64_t>(E) * es / unit : E / unit;
+    q.units_per_row = static_cast<int32_t>(upr);
+    q.dense = (q.tok_stride_b == q.row_src_bytes) && (q.dst_stride_b == q.row_dst_bytes);
+    if (!q.dense) {
+      // the row split divides 32-bit unit indices inside one page
+      if (static_cast<uint64_t>(B) * static_cast<uint64_t>(upr) >= (1ull << 32)) return PMG_ERR_UNSUPPORTED;
+      uint32_t l = 0;
+      while ((1ull << l) < static_cast<uint64_t>(upr)) ++l;
+      const uint64_t m = (((1ull << l) - static_cast<uint64_t>(upr)) << 32) / static_cast<uint64_t>(upr) + 1;
+      q.upr_magic = static_cast<uint32_t>(m);
+      q.upr_shift = static_cast<int32_t>(l);
+    }
+  }
+  return PMG_OK;
+}
+
+// --- per-device launch facts -------------------------------------------------
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int g_sm_count[kMaxDevices];
+bool g_attr_set[kMaxDevices];
+int g_optin_smem[kMaxDevices];
+bool g_plan_attr_set[kMaxDevices];
+
+using KernelFn = void (*)(Params);
+
+KernelFn simt_kernel_for(int conv, int unit) {
+#define PMG_CASE(C, N) \
+  if (conv == C && unit == N) return gather_simt_kernel<C, N>;
+  PMG_CASE(CONV_COPY, 16) PMG_CASE(CONV_COPY, 8) PMG_CASE(CONV_COPY, 4) PMG_CASE(CONV_COPY, 2)
+  PMG_CASE(CONV_COPY, 1)
+  PMG_CASE(CONV_E4M3_BF16, 16) PMG_CASE(CONV_E4M3_BF16, 4) PMG_CASE(CONV_E4M3_BF16, 1)
+  PMG_CASE(CONV_E4M3_F16, 16) PMG_CASE(CONV_E4M3_F16, 4) PMG_CASE(CONV_E4M3_F16, 1)
+  PMG_CASE(CONV_E4M3_F32, 16) PMG_CASE(CONV_E4M3_F32, 4) PMG_CASE(CONV_E4M3_F32, 1)
+  PMG_CASE(CONV_BF16_F32, 8) PMG_CASE(CONV_BF16_F32, 2) PMG_CASE(CONV_BF16_F32, 1)
+  PMG_CASE(CONV_F16_F32, 8) PMG_CASE(CONV_F16_F32, 2) PMG_CASE(CONV_F16_F32, 1)
+#undef PMG_CASE
+  return nullptr;
+}
+
+const KernelFn kAllSimt[] = {
+    gather_simt_kernel<CONV_COPY, 16>,      gather_simt_kernel<CONV_COPY, 8>,      gather_simt_kernel<CONV_COPY, 4>,
+    gather_simt_kernel<CONV_COPY, 2>,       gather_simt_kernel<CONV_COPY, 1>,      gather_simt_kernel<CONV_E4M3_BF16, 16>,
+    gather_simt_kernel<CONV_E4M3_BF16, 4>,  gather_simt_kernel<CONV_E4M3_BF16, 1>, gather_simt_kernel<CONV_E4M3_F16, 16>,
+    gather_simt_kernel<CONV_E4M3_F16, 4>,   gather_simt_kernel<CONV_E4M3_F16, 1>,  gather_simt_kernel<CONV_E4M3_F32, 16>,
+    gather_simt_kernel<CONV_E4M3_F32, 4>,   gather_simt_kernel<CONV_E4M3_F32, 1>,  gather_simt_kernel<CONV_BF16_F32, 8>,
+    gather_simt_kernel<CONV_BF16_F32, 2>,   gather_simt_kernel<CONV_BF16_F32, 1>,  gather_simt_kernel<CONV_F16_F32, 8>,
+    gather_simt_kernel<CONV_F16_F32, 2>,    gather_simt_kernel<CONV_F16_F32, 1>,
+};
+
+// Raises a kernel's dynamic shared memory limit to what the device allows
+// per block beyond the kernel's own static shared memory.
+int allow_max_dyn_smem(KernelFn k, int optin) {
+  cudaFuncAttributes fa;
+  if (cudaFuncGetAttributes(&fa, k) != cudaSuccess) return PMG_ERR_CUDA;
+  const int limit = optin - static_cast<int>(fa.sharedSizeBytes);
+  if (limit <= 0) return PMG_ERR_CUDA;
+  return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, limit) == cudaSuccess ? PMG_OK
+                                                                                                        : PMG_ERR_CUDA;
+}
+
+// SM count of the current device; raises the dynamic shared memory limit of
+// every kernel once per device.
+int device_setup(int* sm_count) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PMG_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return PMG_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_attr_set[dev]) {
+    int n = 0, optin = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return PMG_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return PMG_ERR_CUDA;
+    if (allow_max_dyn_smem(reinterpret_cast<KernelFn>(gather_bulk_kernel), optin) != PMG_OK) return PMG_ERR_CUDA;
+    for (KernelFn k : kAllSimt)
+      if (allow_max_dyn_smem(k, optin) != PMG_OK) return PMG_ERR_CUDA;
+    g_sm_count[dev] = n;
+    g_optin_smem[dev] = optin;
+    g_attr_set[dev] = true;
+  }
+  *sm_count = g_sm_count[dev];
+  return PMG_OK;
+}
+
+size_t host_plan_bytes(int R) { return (static_cast<size_t>(3) * R + 2) * sizeof(int32_t); }
+
+// Resident CTAs per SM for (kernel, block size, dynamic shared memory),
+// memoised per device so repeated calls skip the occupancy query.
+int ctas_per_sm(KernelFn k, int threads, size_t smem, int* out) {
+  struct Entry {
+    int dev;
+    KernelFn k;
+    size_t smem;
+    int n;
+  };
+  static Entry cache[64];
+  static int used = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PMG_ERR_CUDA;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    for (int i = 0; i < used; ++i)
+      if (cache[i].dev == dev && cache[i].k == k && cache[i].smem == smem) {
+        *out = cache[i].n;
+        return PMG_OK;
+      }
+  }
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, threads, smem) != cudaSuccess) return PMG_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (used < 64) cache[used++] = Entry{dev, k, smem, n};
+  *out = n;
+  return PMG_OK;
+}
+
+int launch_gather(const Plan& pl, cudaStream_t stream) {
+  int sms = 0;
+  const int st = device_setup(&sms);
+  if (st != PMG_OK) return st;
+  const Params& q = pl.prm;
+  const int64_t max_by_rows = (static_cast<int64_t>(q.T) + kMinRowsPerCta - 1) / kMinRowsPerCta;
+  if (pl.path == PMG_PATH_BULK) {
+    const size_t smem = static_cast<size_t>(kBulkStages) * q.stage_bytes + host_plan_bytes(q.R);
+    int per_sm = 0;
+    if (ctas_per_sm(gather_bulk_kernel, kBulkThreads, smem, &per_sm) != PMG_OK) return PMG_ERR_CUDA;
+    if (per_sm < 1) return PMG_ERR_UNSUPPORTED;
+    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(static_cast<int64_t>(per_sm) * sms, max_by_rows));
+    gather_bulk_kernel<<<static_cast<unsigned>(grid), kBulkThreads, smem, stream>>>(q);
+  } else {
+    KernelFn k = simt_kernel_for(pl.conv, pl.unit);
+    if (k == nullptr) return PMG_ERR_UNSUPPORTED;
+    const size_t smem = host_plan_bytes(q.R);
+    int per_sm = 0;
+    if (ctas_per_sm(k, kPlanThreads, smem, &per_sm) != PMG_OK) return PMG_ERR_CUDA;
+    if (per_sm < 1) return PMG_ERR_UNSUPPORTED;
+    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(static_cast<int64_t>(per_sm) * sms, max_by_rows));
+    k<<<static_cast<unsigned>(grid), kPlanThreads, smem, stream>>>(q);
+  }
+  return cudaGetLastError() == cudaSuccess ? PMG_OK : PMG_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pmg_gather_ex(const void* cache, int64_t cache_block_stride, int64_t cache_token_stride, int64_t num_blocks,
+                  const int32_t* block_table, int64_t block_table_stride, const int32_t* cu_seq_lens,
+                  const int32_t* seq_starts, int32_t num_reqs, int64_t total_tokens, int32_t block_size,
+                  int32_t entry_size, int32_t src_dtype, int32_t dst_dtype, const float* scale, void* dst,
+                  int64_t dst_token_stride, int32_t* error_flag, void* stream, uint32_t options) {
+  Plan pl;
+  const int st = make_plan(cache, cache_block_stride, cache_token_stride, num_blocks, block_table, block_table_stride,
+                           cu_seq_lens, seq_starts, num_reqs, total_tokens, block_size, entry_size, src_dtype,
+                           dst_dtype, scale, dst, dst_token_stride, error_flag, options, pl);
+  if (st != PMG_OK) return st;
+  if (pl.path == PMG_PATH_NONE) return PMG_OK;
+  return launch_gather(pl, static_cast<cudaStream_t>(stream));
+}
+
+int pmg_gather(const void* cache, int64_t cache_block_stride, int64_t cache_token_stride, int64_t num_blocks,
+               const int32_t* block_table, int64_t block_table_stride, const int32_t* cu_seq_lens,
+               const int32_t* seq_starts, int32_t num_reqs, int64_t total_tokens, int32_t block_size,
+               int32_t entry_size, int32_t src_dtype, int32_t dst_dtype, const float* scale, void* dst,
+               int64_t dst_token_stride, int32_t* error_flag, void* stream) {
+  return pmg_gather_ex(cache, cache_block_stride, cache_token_stride, num_blocks, block_table, block_table_stride,
+                       cu_seq_lens, seq_starts, num_reqs, total_tokens, block_size, entry_size, src_dtype, dst_dtype,
+                       scale, dst, dst_token_stride, error_flag, stream, 0u);
+}
+
+int pmg_select_path(const void* cache, int64_t cache_block_stride, int64_t cache_token_stride, int64_t num_blocks,
+                    const int32_t* block_table, int64_t block_table_stride, const int32_t* cu_seq_lens,
+                    int32_t num_reqs, int64_t total_tokens, int32_t block_size, int32_t entry_size, int32_t src_dtype,
+                    int32_t dst_dtype, const void* dst, int64_t dst_token_stride, uint32_t options, int32_t* path_out,
+                    int32_t* unit_elems_out) {
+  Plan pl;
+  const int st = make_plan(cache, cache_block_stride, cache_token_stride, num_blocks, block_table, block_table_stride,
+                           cu_seq_lens, nullptr, num_reqs, total_tokens, block_size, entry_size, src_dtype, dst_dtype,
+                           nullptr, dst, dst_token_stride, nullptr, options, pl);
+  if (st != PMG_OK) return st;
+  if (path_out) *path_out = pl.path;
+  if (unit_elems_out) {
+    int u = pl.unit;
+    // report elements, not bytes, for a byte copy
+    if (pl.path != PMG_PATH_BULK && pl.path != PMG_PATH_NONE && pl.conv == CONV_COPY) u /= elem_bytes(src_dtype);
+    *unit_elems_out = (pl.path == PMG_PATH_BULK || pl.path == PMG_PATH_NONE) ? 0 : u;
+  }
+  return PMG_OK;
+}
+
+int pmg_debug_plan(const int32_t* cu_seq_lens, const int32_t* seq_starts, int32_t num_reqs, int64_t total_tokens,
+                   int32_t block_size, int32_t* tasks_out, int64_t max_tasks, int64_t* num_tasks_out,
+                   int32_t* error_flag, void* stream, uint32_t options) {
+  if (num_reqs < 0 || total_tokens < 0 || block_size < 1 || max_tasks < 0) return PMG_ERR_ARG;
+  if (options & ~PMG_OPT_IMPLIED_END) return PMG_ERR_ARG;
+  if (num_reqs > PMG_MAX_REQS) return PMG_ERR_UNSUPPORTED;
+  if (num_tasks_out == nullptr || (num_reqs > 0 && cu_seq_lens == nullptr) || (max_tasks > 0 && tasks_out == nullptr))
+    return PMG_ERR_NULL;
+  Params q{};
+  q.cu = cu_seq_lens;
+  q.ss = seq_starts;
+  q.R = num_reqs;
+  q.T = static_cast<int32_t>(total_tokens < INT32_MAX ? total_tokens : INT32_MAX);
+  q.B = block_size;
+  q.implied_end = (options & PMG_OPT_IMPLIED_END) ? 1 : 0;
+  q.err = error_flag;
+  int sms = 0;
+  const int st = device_setup(&sms);
+  if (st != PMG_OK) return st;
+  {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PMG_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_plan_attr_set[dev]) {
+      cudaFuncAttributes fa;
+      if (cudaFuncGetAttributes(&fa, debug_plan_kernel) != cudaSuccess) return PMG_ERR_CUDA;
+      if (cudaFuncSetAttribute(debug_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               g_optin_smem[dev] - static_cast<int>(fa.sharedSizeBytes)) != cudaSuccess)
+        return PMG_ERR_CUDA;
+      g_plan_attr_set[dev] = true;
+    }
+  }
+  debug_plan_kernel<<<1, kPlanThreads, host_plan_bytes(num_reqs), static_cast<cudaStream_t>(stream)>>>(
+      q, tasks_out, max_tasks, num_tasks_out);
+  return cudaGetLastError() == cudaSuccess ? PMG_OK : PMG_ERR_CUDA;
+}
+
+const char* pmg_status_string(int status) {
+  switch (status) {
+    case PMG_OK: return "PMG_OK: success";
+    case PMG_ERR_NULL: return "PMG_ERR_NULL: a required pointer is NULL";
+    case PMG_ERR_ARG: return "PMG_ERR_ARG: a size, stride or option is out of range";
+    case PMG_ERR_DTYPE: return "PMG_ERR_DTYPE: unknown dtype or unsupported (src, dst) pair";
+    case PMG_ERR_ALIGN: return "PMG_ERR_ALIGN: a pointer is not aligned to its element size";
+    case PMG_ERR_UNSUPPORTED: return "PMG_ERR_UNSUPPORTED: request beyond this build's limits";
+    case PMG_ERR_CUDA: return "PMG_ERR_CUDA: a CUDA runtime call or kernel launch failed";
+    default: return "unknown pmg status";
+  }
+}
+
+int pmg_version(void) { return 1; }
+
+}  // extern "C"

@@ -1,0 +1,300 @@
+"""GPU parity: the CUDA gather against the CPU oracle, element by element.
+
+Source of the operation: "MLA cache gather scheduled per logical page"
+(prhub.com.cn, vllm PR #51739): section "关键源码片段" (the uneven-length
+test and the page mapper), section "实现拆解" items 1 and 3 (raw copy, FP8
+upconvert and maybe-dequant; long uneven requests, seq_starts on and off,
+shuffled blocks, partial pages, unaligned strides, zero-length requests) and
+the review section "评论区精华" (block-table bounds and int32 overflow).
+
+Tolerance: 0. Byte copies must match bit for bit; converting gathers must too,
+except that a NaN matches any NaN (no workload below draws NaN codes except
+the all-codes test).
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import gather as og
+from oracle import plan as op
+from paged_mla_kv_cache_gb300 import binding
+from paged_mla_kv_cache_gb300 import workloads as W
+
+from gpu_helpers import DeviceCase, assert_same, oracle_run
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(cuda_lib):
+    if not torch.cuda.is_available():
+        pytest.fail("a GPU test ran without a CUDA device")
+    return cuda_lib
+
+
+def _check(wl, options=0, dst_row_stride=None, expect_flag=0, **kw):
+    case = DeviceCase(wl, dst_row_stride=dst_row_stride, **kw)
+    case.run(options=options)
+    got, flag, guards = case.result()
+    want, oflag = oracle_run(wl, dst_row_stride=dst_row_stride, **{k: v for k, v in kw.items()
+                                                                    if k in ("cu", "seq_starts", "block_table",
+                                                                             "total_tokens")})
+    assert guards, "guard regions around dst were written"
+    assert oflag == expect_flag
+    assert flag == oflag, f"device flag {flag} != oracle flag {oflag}"
+    assert_same(got, want, wl.dst_dtype, wl.src_dtype != wl.dst_dtype)
+    return case
+
+
+# --- the five named workloads at full size, in the launch configuration the
+# benchmark times ------------------------------------------------------------
+
+@pytest.mark.parametrize("name", ["tiny", "60k", "300k", "skew8", "skew64_raw", "skew64_dequant"])
+def test_named_workloads_full_size(name):
+    wl = W.CONFIGS[name]()
+    _check(wl)
+
+
+@pytest.mark.parametrize("name", ["tiny", "60k", "skew8", "skew64_raw"])
+@pytest.mark.parametrize("options", [binding.OPT_FORCE_SIMT, binding.OPT_FORCE_SCALAR])
+def test_named_workloads_other_paths(name, options):
+    _check(W.CONFIGS[name](), options=options)
+
+
+# --- the page's own uneven test ----------------------------------------------
+
+@pytest.mark.parametrize("cache_dtype", ["bf16", "fp8_e4m3"])
+@pytest.mark.parametrize("use_seq_starts", [False, True])
+def test_p1_uneven_lengths(cache_dtype, use_seq_starts):
+    wl = W.p1test(cache_dtype, use_seq_starts)
+    _check(wl)
+
+
+# --- dtype matrix, block sizes, entry sizes, strides --------------------------
+
+PAIRS = [("bf16", "bf16"), ("fp16", "fp16"), ("fp32", "fp32"), ("fp8_e4m3", "fp8_e4m3"), ("u8", "u8"),
+         ("fp8_e4m3", "bf16"), ("fp8_e4m3", "fp16"), ("fp8_e4m3", "fp32"), ("bf16", "fp32"), ("fp16", "fp32")]
+
+
+def _small(seed, src, dst, B, E, row_stride=None, starts=True, R=6, maxlen=None, scale=0.05):
+    rng = np.random.default_rng(seed)
+    maxlen = maxlen or 3 * B + 5
+    lens = [int(x) for x in rng.integers(0, maxlen, R)]
+    lens[int(rng.integers(0, R))] = 0
+    st = [int(x) for x in rng.integers(0, 2 * B + 1, R)] if starts else None
+    return W.make_workload("small", lens, st, B, E, None, src, dst, scale, seed, row_stride=row_stride)
+
+
+@pytest.mark.parametrize("src,dst", PAIRS)
+@pytest.mark.parametrize("B,E", [(1, 576), (16, 7), (64, 576), (128, 8), (16, 512), (64, 656), (3, 1)])
+def test_dtype_block_entry_matrix(src, dst, B, E):
+    wl = _small(hash((src, dst, B, E)) % 10000, src, dst, B, E)
+    _check(wl)
+
+
+@pytest.mark.parametrize("src,dst", PAIRS)
+@pytest.mark.parametrize("options", [0, binding.OPT_FORCE_SIMT, binding.OPT_FORCE_SCALAR])
+def test_padded_rows_both_sides(src, dst, options):
+    """Cache rows padded to 640 elements, dst rows padded to 600."""
+    wl = _small(7, src, dst, 64, 576, row_stride=640, R=5, maxlen=300)
+    _check(wl, options=options, dst_row_stride=600)
+
+
+@pytest.mark.parametrize("row_stride,dst_stride", [(577, None), (576, 579), (581, 583)])
+def test_odd_strides_force_narrow_units(row_stride, dst_stride):
+    wl = _small(11, "bf16", "bf16", 16, 576, row_stride=row_stride, R=4, maxlen=70)
+    _check(wl, dst_row_stride=dst_stride)
+    wl8 = _small(12, "fp8_e4m3", "bf16", 16, 576, row_stride=row_stride, R=4, maxlen=70)
+    _check(wl8, dst_row_stride=dst_stride)
+
+
+@pytest.mark.parametrize("scale", [1.0, 0.05, 0.02, 2.0 ** -12, 1e30, 3.0e-39])
+@pytest.mark.parametrize("dst", ["bf16", "fp16", "fp32"])
+def test_all_fp8_codes(scale, dst):
+    """Every e4m3 code (NaN included) through the dequant path."""
+    codes = np.tile(np.arange(256, dtype=np.uint8), 4)  # 1024 elements: 4 rows of 256
+    cache = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).reshape(4, 1, 256)
+    wl = W.Workload("codes", cache, torch.tensor([[2, 0, 3, 1]], dtype=torch.int32),
+                    torch.tensor([0, 4], dtype=torch.int32), None, [4], 1, 4, 1, 256, "fp8_e4m3", dst, scale)
+    for opt in (0, binding.OPT_FORCE_SCALAR):
+        _check(wl, options=opt)
+
+
+# --- edge cases ---------------------------------------------------------------
+
+def test_many_requests_at_the_limit():
+    rng = np.random.default_rng(3)
+    R = binding.MAX_REQS
+    lens = [int(x) for x in rng.integers(0, 40, R)]
+    starts = [int(x) for x in rng.integers(0, 100, R)]
+    wl = W.make_workload("many", lens, starts, 16, 64, None, "bf16", "bf16", 1.0, 5)
+    _check(wl)
+
+
+def test_single_token_requests_and_zero_lengths():
+    lens = [1, 0, 1, 0, 0, 1, 1, 0]
+    wl = W.make_workload("ones", lens, [63, 5, 0, 0, 1, 64, 127, 3], 64, 576, None, "bf16", "bf16", 1.0, 9)
+    _check(wl)
+
+
+def test_cu_offset_and_clamp_at_total_tokens():
+    wl = W.make_workload("clamp", [100, 50, 70], [5, 0, 9], 16, 576, None, "bf16", "bf16", 1.0, 13, cu_offset=10,
+                         total_tokens=150)
+    _check(wl)
+
+
+def test_empty_calls_write_nothing():
+    wl = W.make_workload("empty", [0, 0, 0], [1, 2, 3], 16, 32, None, "bf16", "bf16", 1.0, 14, total_tokens=8)
+    _check(wl)
+    wl0 = W.make_workload("noreq", [], None, 16, 32, 4, "bf16", "bf16", 1.0, 15, total_tokens=4)
+    _check(wl0)
+    wlT = W.make_workload("zeroT", [5], None, 16, 32, None, "bf16", "bf16", 1.0, 16, total_tokens=0)
+    _check(wlT)
+
+
+def test_non_default_stream():
+    wl = W.skew8()
+    case = DeviceCase(wl)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        case.run(stream=s)
+    s.synchronize()
+    got, flag, guards = case.result()
+    want, oflag = oracle_run(wl)
+    assert guards and flag == oflag == 0
+    assert_same(got, want, "bf16", True)
+
+
+def test_repeated_calls_are_deterministic():
+    wl = W.skew64("dequant")
+    case = DeviceCase(wl)
+    case.run()
+    first, _, _ = case.result()
+    case.dst_full.view(torch.uint8).fill_(0x3C)
+    case.run()
+    second, flag, guards = case.result()
+    assert guards and flag == 0
+    assert np.array_equal(first, second)
+
+
+# --- invalid data: skipped rows, flags, untouched output (review section) -------
+
+def _flag_case(**kw):
+    base = dict(lens=[40, 30, 25], starts=[3, 0, 7], B=16, E=64)
+    base.update(kw)
+    return W.make_workload("flags", base["lens"], base["starts"], base["B"], base["E"], None, "bf16", "bf16", 1.0,
+                           21)
+
+
+def test_logical_block_past_table_row():
+    wl = _flag_case()
+    bt = wl.block_table.numpy().copy()
+    # request 1 (len 30) now starts at 40: its row holds 2 ids in a 3-wide
+    # table, so logical block 2 is the -1 padding and blocks 3, 4 are past the row
+    ss = np.array([3, 40, 7], np.int32)
+    _check(wl, seq_starts=ss, expect_flag=og.BAD_LOGICAL | og.BAD_PHYS)
+
+
+@pytest.mark.parametrize("bad", [-1, 10 ** 6, -(2 ** 31)])
+def test_physical_block_out_of_range(bad):
+    wl = _flag_case()
+    bt = wl.block_table.numpy().copy()
+    bt[1, 1] = bad
+    bt[2, 0] = bad
+    _check(wl, block_table=bt, expect_flag=og.BAD_PHYS)
+
+
+def test_negative_seq_start():
+    wl = _flag_case()
+    _check(wl, seq_starts=np.array([3, -5, 7], np.int32), expect_flag=og.BAD_START)
+
+
+@pytest.mark.parametrize("cu", [[0, 40, 30, 95], [-1, 40, 70, 95], [0, 40, 70, 60]])
+def test_invalid_cu_writes_nothing(cu):
+    wl = _flag_case()
+    _check(wl, cu=np.array(cu, np.int32), expect_flag=og.BAD_CU)
+
+
+def test_huge_seq_start_no_overflow():
+    wl = _flag_case()
+    _check(wl, seq_starts=np.array([3, 2 ** 31 - 10, 7], np.int32), expect_flag=og.BAD_LOGICAL)
+
+
+# --- implied terminal entry (has_terminal_start = false) -----------------------
+
+@pytest.mark.parametrize("T_cut", [0, 7, 27, 40])
+def test_implied_end_convention(T_cut):
+    """cu_seq_lens without its terminal entry: the last request ends at total_tokens."""
+    wl = W.make_workload("implied", [40, 30, 32], [3, 0, 7], 16, 64, None, "bf16", "bf16", 1.0, 31)
+    T = 102 - T_cut
+    cu_short = wl.cu_seq_lens.numpy()[:-1].copy()
+    # the oracle takes the explicit form: the last request ends at total_tokens
+    cu_full = np.concatenate([cu_short, [max(T, int(cu_short[-1]))]]).astype(np.int32)
+    want, oflag = oracle_run(wl, cu=cu_full, total_tokens=T)
+    case = DeviceCase(wl, cu=cu_short, total_tokens=T)
+    case.run(options=binding.OPT_IMPLIED_END)
+    got, flag, guards = case.result()
+    assert guards and oflag == 0 and flag == oflag
+    assert_same(got, want, "bf16", False)
+
+
+# --- the device mapper alone ---------------------------------------------------
+
+def _plan_case(seed):
+    rng = np.random.default_rng(seed)
+    R = int(rng.integers(1, 60))
+    B = int(rng.choice([1, 2, 16, 64]))
+    lens = [int(x) if rng.random() > 0.2 else 0 for x in rng.integers(0, 6 * B + 3, R)]
+    starts = [int(x) for x in rng.integers(0, 3 * B, R)] if rng.random() < 0.6 else None
+    off = int(rng.integers(0, 4))
+    cu = np.concatenate([[off], off + np.cumsum(lens)]).astype(np.int32)
+    T = int(cu[-1]) - int(rng.integers(0, 3))
+    return cu, starts, R, max(T, 0), B
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_debug_plan_matches_oracle_plan(seed):
+    cu, starts, R, T, B = _plan_case(seed)
+    want = op.page_tasks(cu.tolist(), starts, R, T, B)
+    dev = "cuda:0"
+    ss = None if starts is None else torch.tensor(starts, dtype=torch.int32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    tasks, num = binding.debug_plan(torch.from_numpy(cu).to(dev), ss, T, B, len(want) + 3, error_flag=err)
+    assert int(num.item()) == len(want)
+    got = [tuple(int(x) for x in row) for row in tasks.cpu().numpy()[:len(want)]]
+    assert got == want
+    assert np.all(tasks.cpu().numpy()[len(want):] == -1)
+    assert int(err.item()) == 0
+
+
+def test_debug_plan_golden_cases():
+    import json, os
+    cases = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "hand_cases.json")))["cases"]
+    for c in cases:
+        cu = torch.tensor(c["cu_seq_lens"], dtype=torch.int32, device="cuda:0")
+        ss = None if c["seq_starts"] is None else torch.tensor(c["seq_starts"], dtype=torch.int32, device="cuda:0")
+        tasks, num = binding.debug_plan(cu, ss, c["total_tokens"], c["block_size"], 16)
+        n = int(num.item())
+        assert n == len(c["tasks"]), c["name"]
+        assert [list(map(int, r)) for r in tasks.cpu().numpy()[:n]] == c["tasks"], c["name"]
+
+
+# --- 64-bit addressing: output offsets past 2^31 bytes --------------------------
+
+@pytest.mark.slow
+def test_int64_output_offsets_fp32_1m_tokens():
+    """fp32 raw copy of 576-element entries (2304 B) over 1,000,000 tokens: the
+    output byte offset passes 2^31 near token 932,068."""
+    B, E, T = 64, 576, 1_000_000
+    nb = T // B + 2
+    # id-coded values: element (b, s, e) holds b << 16 | s << 10 | e (as fp32 bits)
+    b = np.arange(nb, dtype=np.uint32)[:, None, None]
+    s = np.arange(B, dtype=np.uint32)[None, :, None]
+    e = np.arange(E, dtype=np.uint32)[None, None, :]
+    bits = ((b << 16) | (s << 10) | e).astype(np.uint32)
+    perm = np.random.default_rng(41).permutation(nb).astype(np.int32)
+    cache = torch.from_numpy(bits.view(np.float32))
+    wl = W.Workload("int64", cache, torch.from_numpy(perm[None, :].copy()),
+                    torch.tensor([0, T], dtype=torch.int32), torch.tensor([17], dtype=torch.int32), [T], 1, T, B, E,
+                    "fp32", "fp32", 1.0)
+    _check(wl)
