@@ -160,10 +160,13 @@ def run_ours(args, wl: W.Workload, ws: int, rank: int, local: int):
     nrep = max(2, math.ceil(4 * L2_BYTES / base.nbytes()))
     reps = [base] + [DeviceInputs(wl, dev) for _ in range(nrep - 1)]
 
+    # one scheduling workspace serves every call on this stream
+    ws_buf = None if args.no_workspace else binding.new_workspace(dev)
+
     def step(k, strm=None):
         r = reps[k % nrep]
         binding.gather(r.cache, r.dst, r.bt, r.cu, r.ss, r.scale, r.err, num_reqs=wl.num_reqs,
-                       stream=stream if strm is None else strm, options=args.options)
+                       stream=stream if strm is None else strm, options=args.options, workspace=ws_buf)
 
     path, unit = binding.select_path(base.cache, base.dst, base.bt, base.cu, num_reqs=wl.num_reqs,
                                      options=args.options)
@@ -272,6 +275,7 @@ def run_ours(args, wl: W.Workload, ws: int, rank: int, local: int):
             "cache_dtype": wl.src_dtype,
             "out_dtype": wl.dst_dtype,
             "path": path if args.options == 0 else f"{path} (options {args.options})",
+            "schedule": "static" if args.no_workspace else "dynamic (workspace)",
             "bytes_per_step": alg_bytes,
             "l2": f"{nrep} rotating input replicas ({sum(r.nbytes() for r in reps) / 1e6:.0f} MB) > 4x L2; no flush",
             "parallelism": f"replicas x{ws}",
@@ -312,6 +316,7 @@ def run_e2e(wl, dev, stream, alg_bytes, steps, ws):
     d_scale = torch.empty(1, dtype=torch.float32, device=dev)
     d_out = torch.empty(h_out.shape, dtype=h_out.dtype, device=dev)
     d_err = torch.zeros(1, dtype=torch.int32, device=dev)
+    d_ws = binding.new_workspace(dev)
     h2d = sum(t.numel() * t.element_size() for t in (h_cache, h_bt, h_cu, h_scale) + ((h_ss,) if h_ss is not None else ()))
     d2h = h_out.numel() * h_out.element_size()
 
@@ -323,7 +328,7 @@ def run_e2e(wl, dev, stream, alg_bytes, steps, ws):
             d_ss.copy_(h_ss, non_blocking=True)
         d_scale.copy_(h_scale, non_blocking=True)
         binding.gather(d_cache[:, :, :wl.entry_size], d_out, d_bt, d_cu, d_ss, d_scale, d_err,
-                       num_reqs=wl.num_reqs, stream=stream)
+                       num_reqs=wl.num_reqs, stream=stream, workspace=d_ws)
         h_out.copy_(d_out, non_blocking=True)
 
     for _ in range(2):
@@ -426,6 +431,8 @@ def main():
     ap.add_argument("--config", default="60k", choices=sorted(W.CONFIGS))
     ap.add_argument("--quick", action="store_true", help="skip the cold, e2e and CPU-baseline legs")
     ap.add_argument("--options", type=int, default=0, help="PMG_OPT_* bits passed to every call (path sweeps)")
+    ap.add_argument("--no-workspace", action="store_true",
+                    help="static work split (no scheduling workspace) for comparison")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

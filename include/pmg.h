@@ -123,18 +123,35 @@ int pmg_gather(const void* cache, int64_t cache_block_stride, int64_t cache_toke
                int32_t entry_size, int32_t src_dtype, int32_t dst_dtype, const float* scale, void* dst,
                int64_t dst_token_stride, int32_t* error_flag, void* stream);
 
+/* Size of the scheduling workspace of pmg_gather_ex, in int32 elements. */
+#define PMG_WORKSPACE_INTS 4
+
 /*
- * pmg_gather_ex — pmg_gather with PMG_OPT_* options (0 = pmg_gather).
- * PMG_OPT_IMPLIED_END selects the page's other calling convention
- * (map_gather_page_task with has_terminal_start = false, section
- * "关键源码片段"): cu_seq_lens then holds num_reqs entries and request
- * num_reqs-1 ends at total_tokens.
+ * pmg_gather_ex — pmg_gather with a scheduling workspace and PMG_OPT_* options
+ * (workspace NULL and options 0 is exactly pmg_gather).
+ *
+ *  workspace  device int32 [PMG_WORKSPACE_INTS], 16-byte aligned, or NULL.
+ *             With a workspace, the TMA paths hand out the second half of the
+ *             output rows in small pieces through an atomic counter, so CTAs
+ *             whose memory traffic is served faster take more of the work
+ *             (without one, every CTA gets one equal share). The caller zeroes
+ *             it once before first use; every call that completes leaves it
+ *             zeroed again. Calls that may run concurrently (different
+ *             streams) need separate workspaces: two calls sharing one at the
+ *             same time race. After a call that reported PMG_FLAG_TIMEOUT,
+ *             zero it again. The SIMT paths ignore it.
+ *  options    PMG_OPT_* bits. PMG_OPT_IMPLIED_END selects the page's other
+ *             calling convention (map_gather_page_task with
+ *             has_terminal_start = false, section "关键源码片段"): cu_seq_lens
+ *             then holds num_reqs entries and request num_reqs-1 ends at
+ *             total_tokens.
  */
 int pmg_gather_ex(const void* cache, int64_t cache_block_stride, int64_t cache_token_stride, int64_t num_blocks,
                   const int32_t* block_table, int64_t block_table_stride, const int32_t* cu_seq_lens,
                   const int32_t* seq_starts, int32_t num_reqs, int64_t total_tokens, int32_t block_size,
                   int32_t entry_size, int32_t src_dtype, int32_t dst_dtype, const float* scale, void* dst,
-                  int64_t dst_token_stride, int32_t* error_flag, void* stream, uint32_t options);
+                  int64_t dst_token_stride, int32_t* error_flag, int32_t* workspace, void* stream,
+                  uint32_t options);
 
 /*
  * pmg_select_path — host-only: validates the layout arguments of a gather the

@@ -39,6 +39,7 @@ OPT_FORCE_SCALAR = 2
 OPT_IMPLIED_END = 4
 
 PATH_NAMES = {0: "none", 1: "bulk", 2: "vector", 3: "scalar"}
+WORKSPACE_INTS = 4
 MAX_REQS = 4096
 
 
@@ -71,7 +72,7 @@ def load_library() -> ctypes.CDLL:
         L.pmg_gather.restype = ctypes.c_int
         L.pmg_gather.argtypes = gather_args
         L.pmg_gather_ex.restype = ctypes.c_int
-        L.pmg_gather_ex.argtypes = gather_args + [u32]
+        L.pmg_gather_ex.argtypes = gather_args[:18] + [vp, vp, u32]
         L.pmg_select_path.restype = ctypes.c_int
         L.pmg_select_path.argtypes = [vp, i64, i64, i64, vp, i64, vp, i32, i64, i32, i32, i32, i32, vp, i64, u32,
                                       ctypes.POINTER(i32), ctypes.POINTER(i32)]
@@ -125,7 +126,7 @@ def _layout(cache: torch.Tensor, dst: torch.Tensor):
 def gather(cache: torch.Tensor, dst: torch.Tensor, block_table: torch.Tensor, cu_seq_lens: torch.Tensor,
            seq_starts: Optional[torch.Tensor] = None, scale: Optional[torch.Tensor] = None,
            error_flag: Optional[torch.Tensor] = None, num_reqs: Optional[int] = None, stream=None,
-           options: int = 0) -> None:
+           options: int = 0, workspace: Optional[torch.Tensor] = None) -> None:
     """Gather the cached entries of every request into dst (asynchronous).
 
     cache        [num_blocks, block_size, entry_size] device tensor; a padded
@@ -137,6 +138,8 @@ def gather(cache: torch.Tensor, dst: torch.Tensor, block_table: torch.Tensor, cu
     scale        fp32 device scalar tensor or None (1.0); used for fp8 sources.
     error_flag   int32 device tensor of one element or None.
     num_reqs     defaults to the request count implied by cu_seq_lens.
+    workspace    int32 device tensor of WORKSPACE_INTS zeros (see new_workspace), or
+                 None: dynamic work distribution on the TMA paths.
     """
     src_code, dst_code = _layout(cache, dst)
     if num_reqs is None:
@@ -146,10 +149,16 @@ def gather(cache: torch.Tensor, dst: torch.Tensor, block_table: torch.Tensor, cu
         _ptr(cache), cache.stride(0), cache.stride(1), cache.shape[0],
         _ptr(block_table), bt_stride, _ptr(cu_seq_lens), _ptr(seq_starts), int(num_reqs),
         dst.shape[0], cache.shape[1], cache.shape[2], src_code, dst_code, _ptr(scale),
-        _ptr(dst), dst.stride(0), _ptr(error_flag),
+        _ptr(dst), dst.stride(0), _ptr(error_flag), _ptr(workspace),
         _stream_handle(stream), int(options))
     if st != PMG_OK:
         raise PmgError(st, "pmg_gather")
+
+
+def new_workspace(device) -> torch.Tensor:
+    """A zeroed scheduling workspace for gather(..., workspace=...). One per
+    stream: concurrent calls must not share one."""
+    return torch.zeros(WORKSPACE_INTS, dtype=torch.int32, device=device)
 
 
 def select_path(cache: torch.Tensor, dst: torch.Tensor, block_table: torch.Tensor, cu_seq_lens: torch.Tensor,

@@ -87,6 +87,9 @@ struct Params {
   int64_t dst_stride_b;   // bytes between output rows
   const float* scale;     // may be null
   int32_t* err;           // may be null
+  int32_t* sched;         // work-claim counter in the caller's workspace, or null (static split)
+  int32_t sched_static_pct;  // dynamic mode: share of rows split statically up front
+  int32_t sched_min_rows;    // dynamic mode only when rows per CTA reach this
   // SIMT mover
   int32_t units_per_row;  // entry_size / elements per unit
   uint32_t upr_magic;     // fast division by units_per_row (fast_div)
@@ -111,6 +114,43 @@ __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
+}
+
+// Metadata (cu_seq_lens, seq_starts, block_table) is tiny and read by every
+// CTA, and a serving loop reads the same arrays for every layer: keep it in L2
+// (evict_last) while the entry stream goes through with evict_first.
+__device__ __forceinline__ uint64_t evict_last_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+__device__ __forceinline__ int32_t ld_meta(const int32_t* ptr, uint64_t pol) {
+  int32_t v;
+  asm volatile("ld.global.nc.L2::cache_hint.b32 %0, [%1], %2;" : "=r"(v) : "l"(ptr), "l"(pol));
+  return v;
+}
+
+// The CTAs of a launch together prefetch the whole block table into L2 at
+// entry, so the block-id reads that follow the plan hit L2 instead of waiting
+// on DRAM behind the plan's own reads. Skipped for tables above 4 MB.
+__device__ __forceinline__ void prefetch_block_table(const int32_t* bt, int64_t rows, int64_t stride) {
+  const int64_t bytes = rows * stride * static_cast<int64_t>(sizeof(int32_t));
+  if (bytes <= 0 || bytes > (4ll << 20)) return;
+  const uintptr_t first = reinterpret_cast<uintptr_t>(bt) & ~static_cast<uintptr_t>(127);
+  const uintptr_t last = (reinterpret_cast<uintptr_t>(bt) + static_cast<uintptr_t>(bytes) - 1) & ~static_cast<uintptr_t>(127);
+  const int64_t lines = static_cast<int64_t>((last - first) / 128) + 1;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < lines;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(first + static_cast<uintptr_t>(i) * 128));
+}
+
+// Programmatic dependent launch: let the next kernel in the stream begin its
+// launch now, and wait until the previous kernel's writes are visible before
+// this grid reads any input. Both are no-ops for a normal launch.
+__device__ __forceinline__ void pdl_entry() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -155,14 +195,16 @@ __device__ __forceinline__ PlanView plan_view(uint8_t* base, int R) {
 }
 
 // Pages of request r: the logical blocks its source range [s, s + len) touches
-// (0 for len == 0 or a negative start).
+// (0 for len == 0 or a negative start). With 0 <= s <= 2^31-1 and
+// 1 <= len <= 2^31-1, s + len - 1 < 2^32, so 32-bit unsigned division is exact.
 __device__ __forceinline__ int32_t request_pages(const PlanView& v, int r, int B) {
-  const int64_t len = static_cast<int64_t>(v.ob[r + 1]) - v.ob[r];
-  const int64_t s = v.st[r];
+  const int32_t len = v.ob[r + 1] - v.ob[r];
+  const int32_t s = v.st[r];
   if (len <= 0 || s < 0) return 0;
-  const int64_t first = s / B;
-  const int64_t last_excl = (s + len + B - 1) / B;
-  return static_cast<int32_t>(last_excl - first);
+  const uint32_t ub = static_cast<uint32_t>(B);
+  const uint32_t first = static_cast<uint32_t>(s) / ub;
+  const uint32_t last = (static_cast<uint32_t>(s) + static_cast<uint32_t>(len) - 1u) / ub;
+  return static_cast<int32_t>(last - first + 1u);
 }
 
 // Builds the plan with all threads of the CTA. Returns the number of page
@@ -179,21 +221,23 @@ __device__ int build_plan(const Params& p, const PlanView& v, bool report_flags)
 
   int bad = 0;
   int bad_start = 0;
+  const uint64_t keep = evict_last_policy();
+  if (p.bt != nullptr) prefetch_block_table(p.bt, R, p.bt_stride);
   for (int r = tid; r <= R; r += nt) {
     int64_t c;
     if (p.implied_end && r == R) {
-      const int64_t prev = R > 0 ? static_cast<int64_t>(__ldg(p.cu + R - 1)) : 0;
+      const int64_t prev = R > 0 ? static_cast<int64_t>(ld_meta(p.cu + R - 1, keep)) : 0;
       c = prev > T ? prev : T;
     } else {
-      c = __ldg(p.cu + r);
+      c = ld_meta(p.cu + r, keep);
     }
     if (r == 0 && c < 0) bad = 1;
-    if (r > 0) {
-      const int64_t prev = __ldg(p.cu + r - 1);
+    if (r > 0 && !(p.implied_end && r == R)) {
+      const int64_t prev = ld_meta(p.cu + r - 1, keep);
       if (c < prev) bad = 1;
     }
     v.ob[r] = static_cast<int32_t>(c < T ? c : T);
-    if (r < R) v.st[r] = p.ss ? __ldg(p.ss + r) : 0;
+    if (r < R) v.st[r] = p.ss ? ld_meta(p.ss + r, keep) : 0;
   }
   if (__syncthreads_or(bad)) {
     if (report_flags && tid == 0) set_flag(p, PMG_FLAG_CU_ORDER);
@@ -253,11 +297,11 @@ struct PageTask {
 // the page's clipping of [start, start + len) to logical block lb.
 __device__ __forceinline__ PageTask map_task(const PlanView& v, int R, int B, int32_t t) {
   const int r = upper_bound_i32(v.P, R + 1, t) - 1;
-  const int64_t j = static_cast<int64_t>(t) - v.P[r];
+  const uint32_t j = static_cast<uint32_t>(t - v.P[r]);
   const int64_t s = v.st[r];
   const int64_t len = static_cast<int64_t>(v.ob[r + 1]) - v.ob[r];
-  const int64_t lb = s / B + j;
-  const int64_t page_begin = lb * B;
+  const uint32_t lb = static_cast<uint32_t>(s) / static_cast<uint32_t>(B) + j;  // s >= 0 for any request with pages
+  const int64_t page_begin = static_cast<int64_t>(lb) * B;
   const int64_t cb = s > page_begin ? s : page_begin;
   const int64_t ce = (s + len) < (page_begin + B) ? (s + len) : (page_begin + B);
   PageTask k;
@@ -269,6 +313,15 @@ __device__ __forceinline__ PageTask map_task(const PlanView& v, int R, int B, in
   return k;
 }
 
+// First task whose rows reach output row `row` (row inside [ob[0], ob[R])).
+__device__ __forceinline__ int32_t first_task_for_row(const PlanView& v, int R, int B, uint32_t row) {
+  const int r = upper_bound_i32(v.ob, R + 1, static_cast<int64_t>(row)) - 1;
+  const int32_t s = v.st[r];
+  if (s < 0) return v.P[r];  // no task in r; the next request's tasks follow
+  const uint32_t pos = static_cast<uint32_t>(s) + (row - static_cast<uint32_t>(v.ob[r]));
+  return v.P[r] + static_cast<int32_t>(pos / static_cast<uint32_t>(B) - static_cast<uint32_t>(s) / static_cast<uint32_t>(B));
+}
+
 // The CTA's share of output rows [row0, row1) and its first task id.
 struct CtaRange {
   int32_t row0, row1, t0;
@@ -276,22 +329,17 @@ struct CtaRange {
 
 __device__ __forceinline__ CtaRange cta_range(const PlanView& v, int R, int B, int32_t num_tasks) {
   CtaRange c;
-  const int64_t lo = v.ob[0];
-  const int64_t hi = v.ob[R];
-  const int64_t rows = hi - lo;
-  c.row0 = static_cast<int32_t>(lo + rows * blockIdx.x / gridDim.x);
-  c.row1 = static_cast<int32_t>(lo + rows * (blockIdx.x + 1) / gridDim.x);
+  // balanced split of [lo, hi): the first `rem` CTAs take one row more
+  const uint32_t lo = static_cast<uint32_t>(v.ob[0]);
+  const uint32_t rows = static_cast<uint32_t>(v.ob[R]) - lo;
+  const uint32_t per = rows / gridDim.x;
+  const uint32_t rem = rows - per * gridDim.x;
+  const uint32_t b = blockIdx.x;
+  c.row0 = static_cast<int32_t>(lo + b * per + (b < rem ? b : rem));
+  c.row1 = c.row0 + static_cast<int32_t>(per + (b < rem ? 1u : 0u));
   c.t0 = num_tasks;
   if (c.row0 >= c.row1 || num_tasks <= 0) return c;
-  // request containing row0: last r with ob[r] <= row0 (it is non-empty)
-  const int r = upper_bound_i32(v.ob, R + 1, c.row0) - 1;
-  const int64_t s = v.st[r];
-  if (s < 0) {
-    c.t0 = v.P[r];  // no task in r; start with the next request's tasks
-  } else {
-    const int64_t pos = s + (c.row0 - v.ob[r]);
-    c.t0 = v.P[r] + static_cast<int32_t>(pos / B - s / B);
-  }
+  c.t0 = first_task_for_row(v, R, B, static_cast<uint32_t>(c.row0));
   return c;
 }
 
@@ -323,7 +371,7 @@ __device__ __forceinline__ bool resolve_segment(const Params& p, const PlanView&
     set_flag(p, PMG_FLAG_LOGICAL_BLOCK);
     return true;
   }
-  const int64_t phys = __ldg(p.bt + static_cast<int64_t>(k.req) * p.bt_stride + k.logical_block);
+  const int64_t phys = ld_meta(p.bt + static_cast<int64_t>(k.req) * p.bt_stride + k.logical_block, evict_last_policy());
   if (phys < 0 || phys >= p.num_blocks) {
     set_flag(p, PMG_FLAG_PHYS_BLOCK);
     return true;
@@ -412,7 +460,7 @@ struct Chunk {
   int32_t nrows;
 };
 
-// Walks the segment table chunk by chunk (at most rows_per_stage rows each).
+// Walks a segment table chunk by chunk (at most rows_per_stage rows each).
 struct ChunkIter {
   int seg;
   int32_t row;
@@ -433,99 +481,285 @@ struct ChunkIter {
   }
 };
 
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Work items. Without a workspace, CTA c owns one balanced share of the output
+// rows (static). With a workspace, item c < G is CTA c's static first share (a
+// rows; half of all rows together) and items >= G (d rows each) are claimed in
+// order through an atomic counter, so CTAs that get their data faster take more
+// of the rest; the last CTA to finish resets the counter for the next call.
+// ---------------------------------------------------------------------------
+
+struct Items {
+  uint32_t lo, hi;  // output rows [lo, hi)
+  uint32_t a, d;    // static share and dynamic item size
+  uint32_t n;       // number of items
+  bool dynamic;
+};
+
+// Dynamic mode needs a workspace and enough rows per CTA for the claims to
+// pay off; the static share is sched_static_pct % of the rows, dynamic items
+// are about rows / (16 G) rows and never smaller than one ring stage.
+__device__ __forceinline__ Items make_items(const PlanView& v, const Params& p) {
+  Items it;
+  it.lo = static_cast<uint32_t>(v.ob[0]);
+  it.hi = static_cast<uint32_t>(v.ob[p.R]);
+  const uint32_t rows = it.hi - it.lo;
+  const uint32_t G = gridDim.x;
+  it.dynamic = p.sched != nullptr && rows / G >= static_cast<uint32_t>(p.sched_min_rows);
+  if (it.dynamic) {
+    it.a = static_cast<uint32_t>(static_cast<uint64_t>(rows) * static_cast<uint32_t>(p.sched_static_pct) / 100u / G);
+    const uint32_t d = rows / (16u * G);
+    const uint32_t dmin = static_cast<uint32_t>(p.rows_per_stage > 0 ? p.rows_per_stage : 1);
+    it.d = d > dmin ? d : dmin;
+    const uint32_t rest = rows - G * it.a;
+    it.n = G + (rest + it.d - 1u) / it.d;
+  } else {
+    it.a = it.d = 0;
+    it.n = G;
+  }
+  return it;
+}
+
+__device__ __forceinline__ void item_rows(const Items& it, uint32_t k, uint32_t& r0, uint32_t& r1) {
+  const uint32_t G = gridDim.x;
+  if (!it.dynamic) {
+    const uint32_t rows = it.hi - it.lo;
+    const uint32_t per = rows / G;
+    const uint32_t rem = rows - per * G;
+    r0 = it.lo + k * per + (k < rem ? k : rem);
+    r1 = r0 + per + (k < rem ? 1u : 0u);
+  } else if (k < G) {
+    r0 = it.lo + k * it.a;
+    r1 = r0 + it.a;
+  } else {
+    r0 = it.lo + G * it.a + (k - G) * it.d;
+    r1 = r0 + it.d < it.hi ? r0 + it.d : it.hi;
+  }
+}
+
+// Segment batches handed from the scheduler warp to the producer thread.
+constexpr int kSegBufs = 2;
+constexpr int kSegCap = 32;
+
+struct SegQueue {
+  Segment seg[kSegBufs][kSegCap];
+  int32_t count[kSegBufs];  // -1: no more work
+  uint64_t full[kSegBufs];
+  uint64_t empty[kSegBufs];
+};
+
+__device__ __forceinline__ void segq_init(SegQueue& q) {
+  for (int b = 0; b < kSegBufs; ++b) {
+    mbar_init(&q.full[b], 1);
+    mbar_init(&q.empty[b], 1);
+  }
+}
+
+// The scheduler warp: takes items (its static one, then claimed ones) and
+// resolves each into batches of up to 32 segments, one task per lane (map,
+// block-table read, bounds checks). Returns false on a timeout.
+__device__ bool run_scheduler(const Params& p, const PlanView& v, int32_t num_tasks, const Items& its, SegQueue& q) {
+  const int lane = threadIdx.x & 31;
+  uint32_t uses = 0;
+  uint32_t k = blockIdx.x;
+  bool have = k < its.n;
+  while (have) {
+    // claim the next item now; its latency overlaps this item's resolution
+    uint32_t claimed = 0;
+    if (its.dynamic && lane == 0) claimed = gridDim.x + atomicAdd(reinterpret_cast<unsigned*>(p.sched), 1u);
+    uint32_t r0, r1;
+    item_rows(its, k, r0, r1);
+    if (r0 < r1) {
+      int32_t t = first_task_for_row(v, p.R, p.B, r0);
+      for (;;) {
+        Segment seg;
+        const bool act = resolve_segment(p, v, t + lane, num_tasks, static_cast<int32_t>(r0),
+                                         static_cast<int32_t>(r1), seg);
+        const int n = __popc(__ballot_sync(0xffffffffu, act));
+        if (n == 0) break;
+        const int b = static_cast<int>(uses % kSegBufs);
+        if (uses >= kSegBufs && !mbar_wait_bounded(&q.empty[b], ((uses / kSegBufs) - 1u) & 1u)) return false;
+        q.seg[b][lane] = seg;
+        if (lane == 0) q.count[b] = n;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&q.full[b]);
+        ++uses;
+        if (n < kSegCap) break;
+        t += kSegCap;
+      }
+    }
+    if (its.dynamic) {
+      k = __shfl_sync(0xffffffffu, claimed, 0);
+      have = k < its.n;
+      // Every CTA claims until a claim fails, so a launch makes exactly n
+      // claims in all (n - G that succeed, one failing claim per CTA). The CTA
+      // holding the n-th claim is the last to touch the counter: it resets
+      // the workspace for the next call.
+      if (lane == 0 && k - gridDim.x == its.n - 1u) atomicExch(reinterpret_cast<unsigned*>(p.sched), 0u);
+    } else {
+      have = false;
+    }
+  }
+  const int b = static_cast<int>(uses % kSegBufs);
+  if (uses >= kSegBufs && !mbar_wait_bounded(&q.empty[b], ((uses / kSegBufs) - 1u) & 1u)) return false;
+  if (lane == 0) q.count[b] = -1;
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&q.full[b]);
+  return true;
+}
+
+// Producer-side reader of the segment batches, chunk by chunk.
+struct SegReader {
+  uint32_t uses;
+  int cur;
+  int n;
+  ChunkIter it;
+  bool end;
+  // 1: a chunk; 0: none ready yet (only when block is false); -1: no more work;
+  // -2: a bounded wait ran out
+  __device__ __forceinline__ int next(SegQueue& q, const Params& p, Chunk& c, bool block) {
+    for (;;) {
+      if (cur >= 0) {
+        if (it.next(q.seg[cur], n, p.rows_per_stage, p, c)) return 1;
+        mbar_arrive(&q.empty[cur]);  // chunk descriptors are copied out: the batch is free
+        ++uses;
+        cur = -1;
+      }
+      if (end) return -1;
+      const int b = static_cast<int>(uses % kSegBufs);
+      const uint32_t par = (uses / kSegBufs) & 1u;
+      if (!block) {
+        if (!mbar_test_wait(&q.full[b], par)) return 0;
+      } else if (!mbar_wait_bounded(&q.full[b], par)) {
+        end = true;
+        return -2;
+      }
+      n = q.count[b];
+      if (n < 0) {
+        end = true;
+        return -1;
+      }
+      cur = b;
+      it = ChunkIter{0, 0};
+    }
+  }
+};
+
+__device__ __forceinline__ void issue_loads(const Params& p, const Chunk& c, uint8_t* buf, uint64_t* bar,
+                                            uint64_t pol) {
+  const uint32_t row_bytes = static_cast<uint32_t>(p.row_src_bytes);
+  const uint32_t bytes = static_cast<uint32_t>(c.nrows) * row_bytes;
+  mbar_arrive_expect_tx(bar, bytes);
+  if (p.src_dense) {
+    bulk_load(buf, p.cache + c.src, bytes, bar, pol);
+  } else {
+    for (int32_t i = 0; i < c.nrows; ++i)
+      bulk_load(buf + static_cast<size_t>(i) * row_bytes, p.cache + c.src + i * p.tok_stride_b, row_bytes, bar, pol);
+  }
+}
+
+// Byte copy: warp 0 lane 0 loads chunks into a ring of kBulkStages stages and
+// stores each landed stage straight back out; warp 1 schedules.
 __global__ void __launch_bounds__(kBulkThreads) gather_bulk_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t full_bar[kBulkStages];
   __shared__ Chunk stage_chunk[kBulkStages];
-  __shared__ Segment segs[kBulkThreads];
-  __shared__ int abort_flag;
+  __shared__ __align__(8) SegQueue q;
 
   // layout: [stages][plan]; stage buffers first keeps them 128-byte aligned
   uint8_t* stage_base = smem;
   const PlanView v = plan_view(smem + static_cast<size_t>(kBulkStages) * p.stage_bytes, p.R);
 
+  pdl_entry();
   const int32_t num_tasks = build_plan(p, v, blockIdx.x == 0);
   if (num_tasks <= 0) return;
-  const CtaRange range = cta_range(v, p.R, p.B, num_tasks);
-  if (range.row0 >= range.row1) return;
+  const Items its = make_items(v, p);
 
   const int tid = threadIdx.x;
+  const int warp = tid >> 5;
   if (tid == 0) {
     for (int s = 0; s < kBulkStages; ++s) mbar_init(&full_bar[s], 1);
+    segq_init(q);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    abort_flag = 0;
   }
   __syncthreads();
 
-  const uint64_t pol = evict_first_policy();
-  const uint32_t row_bytes = static_cast<uint32_t>(p.row_src_bytes);
-  uint32_t loads = 0, stores = 0;  // chunks loaded / stored so far (tid 0 only)
-
-  for (int32_t tb = range.t0;; tb += kBulkThreads) {
-    Segment seg;
-    const bool active = resolve_segment(p, v, tb + tid, num_tasks, range.row0, range.row1, seg);
-    segs[tid] = seg;
-    const int nseg = __syncthreads_count(active);
-    if (tid == 0 && nseg > 0) {
-      ChunkIter li{0, 0};
-      bool more = true;
-      bool ok = true;
-      while (ok) {
-        // keep up to kBulkStages chunks loading ahead of the stores
-        while (more && loads - stores < static_cast<uint32_t>(kBulkStages)) {
-          Chunk c;
-          more = li.next(segs, nseg, p.rows_per_stage, p, c);
-          if (!more) break;
-          const int s = static_cast<int>(loads % kBulkStages);
-          if (loads >= static_cast<uint32_t>(kBulkStages)) {
-            // the store that last used stage s must have finished reading it
-            bulk_wait_read_upto(static_cast<int>(stores - 1 - (loads - kBulkStages)));
-          }
-          stage_chunk[s] = c;
-          uint8_t* buf = stage_base + static_cast<size_t>(s) * p.stage_bytes;
-          const uint32_t bytes = static_cast<uint32_t>(c.nrows) * row_bytes;
-          mbar_arrive_expect_tx(&full_bar[s], bytes);
-          if (p.src_dense) {
-            bulk_load(buf, p.cache + c.src, bytes, &full_bar[s], pol);
-          } else {
-            for (int32_t i = 0; i < c.nrows; ++i)
-              bulk_load(buf + static_cast<size_t>(i) * row_bytes, p.cache + c.src + i * p.tok_stride_b, row_bytes,
-                        &full_bar[s], pol);
-          }
-          ++loads;
-        }
-        if (stores == loads) break;
-        const int s = static_cast<int>(stores % kBulkStages);
-        if (!mbar_wait_bounded(&full_bar[s], (stores / kBulkStages) & 1u)) {
-          ok = false;
+  if (warp == 1) {
+    if (!run_scheduler(p, v, num_tasks, its, q)) set_flag(p, PMG_FLAG_TIMEOUT);
+  } else if (tid == 0) {
+    const uint64_t pol = evict_first_policy();
+    const uint32_t row_bytes = static_cast<uint32_t>(p.row_src_bytes);
+    SegReader rd{0, -1, 0, ChunkIter{0, 0}, false};
+    uint32_t loads = 0, stores = 0;
+    bool gen_done = false;
+    bool ok = true;
+    for (;;) {
+      // keep up to kBulkStages chunks loading ahead of the stores
+      while (!gen_done && loads - stores < static_cast<uint32_t>(kBulkStages)) {
+        Chunk c;
+        const int r = rd.next(q, p, c, loads == stores);
+        if (r == 0) break;
+        if (r < 0) {
+          gen_done = true;
+          if (r == -2) ok = false;
           break;
         }
-        const Chunk c = stage_chunk[s];
-        const uint8_t* buf = stage_base + static_cast<size_t>(s) * p.stage_bytes;
-        if (p.dst_dense) {
-          bulk_store(p.dst + c.dst, buf, static_cast<uint32_t>(c.nrows) * row_bytes);
-        } else {
-          for (int32_t i = 0; i < c.nrows; ++i)
-            bulk_store(p.dst + c.dst + i * p.dst_stride_b, buf + static_cast<size_t>(i) * row_bytes, row_bytes);
+        const int s = static_cast<int>(loads % kBulkStages);
+        if (loads >= static_cast<uint32_t>(kBulkStages)) {
+          // the store that last used stage s must have finished reading it
+          bulk_wait_read_upto(static_cast<int>(stores - 1 - (loads - kBulkStages)));
         }
-        bulk_commit();
-        ++stores;
+        stage_chunk[s] = c;
+        issue_loads(p, c, stage_base + static_cast<size_t>(s) * p.stage_bytes, &full_bar[s], pol);
+        ++loads;
       }
-      if (!ok) {
-        // a load never completed: report, give the other loads in flight a
-        // bounded chance to land, then stop this CTA
-        set_flag(p, PMG_FLAG_TIMEOUT);
-        for (uint32_t k = stores + 1; k < loads; ++k)
-          (void)mbar_wait_bounded(&full_bar[k % kBulkStages], (k / kBulkStages) & 1u);
-        abort_flag = 1;
+      if (stores == loads) {
+        if (gen_done) break;
+        continue;
       }
+      const int s = static_cast<int>(stores % kBulkStages);
+      if (!mbar_wait_bounded(&full_bar[s], (stores / kBulkStages) & 1u)) {
+        ok = false;
+        break;
+      }
+      const Chunk c = stage_chunk[s];
+      const uint8_t* buf = stage_base + static_cast<size_t>(s) * p.stage_bytes;
+      if (p.dst_dense) {
+        bulk_store(p.dst + c.dst, buf, static_cast<uint32_t>(c.nrows) * row_bytes);
+      } else {
+        for (int32_t i = 0; i < c.nrows; ++i)
+          bulk_store(p.dst + c.dst + i * p.dst_stride_b, buf + static_cast<size_t>(i) * row_bytes, row_bytes);
+      }
+      bulk_commit();
+      ++stores;
     }
-    const bool last = nseg < kBulkThreads;
-    __syncthreads();
-    if (last || abort_flag) break;
+    if (!ok) {
+      // a wait ran out: report, give the loads in flight a bounded chance to
+      // land, then stop
+      set_flag(p, PMG_FLAG_TIMEOUT);
+      for (uint32_t k = stores + 1; k < loads; ++k)
+        (void)mbar_wait_bounded(&full_bar[k % kBulkStages], (k / kBulkStages) & 1u);
+    }
+    bulk_wait_all();
   }
-  if (tid == 0) bulk_wait_all();
+  __syncthreads();
 }
 
 // ---------------------------------------------------------------------------
@@ -674,6 +908,7 @@ __global__ void __launch_bounds__(kPlanThreads) gather_simt_kernel(const __grid_
   __shared__ int64_t warp_units[kPlanThreads / 32];
 
   const PlanView v = plan_view(smem, p.R);
+  pdl_entry();
   const int32_t num_tasks = build_plan(p, v, blockIdx.x == 0);
   if (num_tasks <= 0) return;
   const CtaRange range = cta_range(v, p.R, p.B, num_tasks);
@@ -759,6 +994,125 @@ __global__ void __launch_bounds__(kPlanThreads) gather_simt_kernel(const __grid_
 }
 
 // ---------------------------------------------------------------------------
+// TMA-in converting path: bulk loads of source rows into a shared-memory ring,
+// converter warps turn each landed stage into destination elements and store
+// them with one coalesced 16-byte store per thread.
+// ---------------------------------------------------------------------------
+
+constexpr int kCvtWarps = 4;                        // converter warps
+constexpr int kCvtThreads = 32 * (kCvtWarps + 2);   // + producer warp + scheduler warp
+constexpr int kCvtStages = 4;
+
+template <int BYTES>
+__device__ __forceinline__ void load_smem(const uint8_t* src, Raw<BYTES>& r) {
+  if constexpr (BYTES == 8) {
+    const uint2 x = *reinterpret_cast<const uint2*>(src);
+    r.w[0] = x.x; r.w[1] = x.y;
+  } else {
+    static_assert(BYTES == 4, "unit size");
+    r.w[0] = *reinterpret_cast<const uint32_t*>(src);
+  }
+}
+
+template <int CONV, int N>
+__global__ void __launch_bounds__(kCvtThreads) gather_tma_convert_kernel(const __grid_constant__ Params p) {
+  constexpr int kInBytes = N * ConvTraits<CONV>::es;
+  constexpr int kOutBytes = N * ConvTraits<CONV>::ed;
+  static_assert(kOutBytes == 16, "one 16-byte store per unit");
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t full_bar[kCvtStages];
+  __shared__ __align__(8) uint64_t empty_bar[kCvtStages];
+  __shared__ Chunk stage_chunk[kCvtStages];
+  __shared__ __align__(8) SegQueue q;
+
+  uint8_t* stage_base = smem;
+  const PlanView v = plan_view(smem + static_cast<size_t>(kCvtStages) * p.stage_bytes, p.R);
+  pdl_entry();
+  const int32_t num_tasks = build_plan(p, v, blockIdx.x == 0);
+  if (num_tasks <= 0) return;
+  const Items its = make_items(v, p);
+
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  if (tid == 0) {
+    for (int s = 0; s < kCvtStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], kCvtWarps);
+    }
+    segq_init(q);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  __syncthreads();
+
+  if (warp == kCvtWarps + 1) {
+    if (!run_scheduler(p, v, num_tasks, its, q)) set_flag(p, PMG_FLAG_TIMEOUT);
+  } else if (warp == kCvtWarps) {
+    // producer: one lane issues the bulk loads, up to kCvtStages chunks ahead
+    if (lane == 0) {
+      const uint64_t pol = evict_first_policy();
+      SegReader rd{0, -1, 0, ChunkIter{0, 0}, false};
+      for (uint32_t g = 0;; ++g) {
+        Chunk c;
+        const int r = rd.next(q, p, c, true);
+        const int s = static_cast<int>(g % kCvtStages);
+        const uint32_t use = g / kCvtStages;
+        if (use > 0 && !mbar_wait_bounded(&empty_bar[s], (use - 1) & 1u)) {
+          set_flag(p, PMG_FLAG_TIMEOUT);
+          break;
+        }
+        if (r <= 0) {
+          // no more work: an empty chunk tells the converters to stop
+          if (r == -2) set_flag(p, PMG_FLAG_TIMEOUT);
+          stage_chunk[s].nrows = 0;
+          mbar_arrive(&full_bar[s]);
+          break;
+        }
+        stage_chunk[s] = c;
+        issue_loads(p, c, stage_base + static_cast<size_t>(s) * p.stage_bytes, &full_bar[s], pol);
+      }
+    }
+  } else {
+    // converters: every landed stage, unit u = (row, col) of the chunk
+    float scale = 1.0f;
+    if (CONV == CONV_E4M3_BF16 || CONV == CONV_E4M3_F16 || CONV == CONV_E4M3_F32) {
+      if (p.scale != nullptr) scale = __ldg(p.scale);
+    }
+    const uint32_t upr = static_cast<uint32_t>(p.units_per_row);
+    for (uint32_t g = 0;; ++g) {
+      const int s = static_cast<int>(g % kCvtStages);
+      if (!mbar_wait_bounded(&full_bar[s], (g / kCvtStages) & 1u)) {
+        set_flag(p, PMG_FLAG_TIMEOUT);
+        break;
+      }
+      const Chunk c = stage_chunk[s];
+      if (c.nrows == 0) break;
+      const uint8_t* in = stage_base + static_cast<size_t>(s) * p.stage_bytes;
+      const uint32_t units = static_cast<uint32_t>(c.nrows) * upr;
+      uint8_t* out = p.dst + c.dst;
+      for (uint32_t u = tid; u < units; u += kCvtWarps * 32) {
+        Raw<kInBytes> x;
+        load_smem<kInBytes>(in + static_cast<size_t>(u) * kInBytes, x);
+        Raw<kOutBytes> y;
+        convert_unit<CONV, N>(x, y, scale);
+        int64_t off;
+        if (p.dense) {
+          off = static_cast<int64_t>(u) * kOutBytes;
+        } else {
+          const uint32_t row = fast_div(u, p.upr_magic, p.upr_shift);
+          off = static_cast<int64_t>(row) * p.dst_stride_b + static_cast<int64_t>(u - row * upr) * kOutBytes;
+        }
+        store_raw<kOutBytes>(out + off, y);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[s]);
+    }
+  }
+  __syncthreads();
+}
+
+// ---------------------------------------------------------------------------
 // Debug plan: the mapper alone
 // ---------------------------------------------------------------------------
 
@@ -825,6 +1179,47 @@ int bulk_stage_target_bytes() {
   return v;
 }
 
+// Target bytes (of source rows) of one stage of the converting TMA ring;
+// PMG_CVT_STAGE_KB (4..48) overrides the default for tuning sweeps.
+int cvt_stage_target_bytes() {
+  static const int v = [] {
+    const char* e = std::getenv("PMG_CVT_STAGE_KB");
+    int kb = e ? std::atoi(e) : 16;
+    if (kb < 4) kb = 4;
+    if (kb > kMaxStageBytes / 1024) kb = kMaxStageBytes / 1024;
+    return kb * 1024;
+  }();
+  return v;
+}
+
+// Dynamic scheduling knobs (PMG_SCHED_STATIC_PCT, PMG_SCHED_MIN_ROWS) for
+// tuning sweeps; they change only the work split, never the result.
+int env_int(const char* name, int dflt, int lo, int hi) {
+  const char* e = std::getenv(name);
+  int v = e ? std::atoi(e) : dflt;
+  return v < lo ? lo : (v > hi ? hi : v);
+}
+int sched_static_pct() {
+  static const int v = env_int("PMG_SCHED_STATIC_PCT", 50, 0, 100);
+  return v;
+}
+int sched_min_rows() {
+  static const int v = env_int("PMG_SCHED_MIN_ROWS", 128, 1, 1 << 30);
+  return v;
+}
+
+// Elements per unit of the converting TMA path: one 16-byte store per unit.
+int tma_convert_unit(int conv) {
+  switch (conv) {
+    case CONV_E4M3_BF16:
+    case CONV_E4M3_F16: return 8;
+    case CONV_E4M3_F32:
+    case CONV_BF16_F32:
+    case CONV_F16_F32: return 4;
+    default: return 0;
+  }
+}
+
 bool aligned(const void* ptr, int64_t a) { return (reinterpret_cast<uintptr_t>(ptr) % static_cast<uint64_t>(a)) == 0; }
 
 struct Plan {
@@ -848,8 +1243,8 @@ int unit_candidates(int conv, int* out) {
 // Validation and path choice: the host half of every entry point. No CUDA call.
 int make_plan(const void* cache, int64_t cbs, int64_t cts, int64_t num_blocks, const int32_t* bt, int64_t bt_stride,
               const int32_t* cu, const int32_t* ss, int32_t R, int64_t T, int32_t B, int32_t E, int32_t sdt,
-              int32_t ddt, const float* scale, const void* dst, int64_t dts, int32_t* err, uint32_t options,
-              Plan& out) {
+              int32_t ddt, const float* scale, const void* dst, int64_t dts, int32_t* err, int32_t* workspace,
+              uint32_t options, Plan& out) {
   out.path = PMG_PATH_NONE;
   out.unit = 0;
   const int conv = conv_of(sdt, ddt);
@@ -867,7 +1262,7 @@ int make_plan(const void* cache, int64_t cbs, int64_t cts, int64_t num_blocks, c
   if (cache == nullptr || bt == nullptr || cu == nullptr || dst == nullptr) return PMG_ERR_NULL;
   if (!aligned(cache, es) || !aligned(dst, ed) || !aligned(bt, 4) || !aligned(cu, 4) ||
       (ss != nullptr && !aligned(ss, 4)) || (scale != nullptr && !aligned(scale, 4)) ||
-      (err != nullptr && !aligned(err, 4)))
+      (err != nullptr && !aligned(err, 4)) || (workspace != nullptr && !aligned(workspace, 16)))
     return PMG_ERR_ALIGN;
   // strides in bytes must not overflow int64
   if (cbs > INT64_MAX / es / 2 || cts > INT64_MAX / es / 2 || dts > INT64_MAX / ed / 2) return PMG_ERR_ARG;
@@ -892,6 +1287,9 @@ int make_plan(const void* cache, int64_t cbs, int64_t cts, int64_t num_blocks, c
   q.dst_stride_b = dts * ed;
   q.scale = scale;
   q.err = err;
+  q.sched = workspace;
+  q.sched_static_pct = sched_static_pct();
+  q.sched_min_rows = sched_min_rows();
   out.conv = conv;
 
   // largest access unit every row start and row length allows
@@ -914,25 +1312,43 @@ int make_plan(const void* cache, int64_t cbs, int64_t cts, int64_t num_blocks, c
   if (options & PMG_OPT_FORCE_SCALAR) unit = (conv == CONV_COPY) ? es : 1;
   out.unit = unit;
 
-  const bool bulk_ok = conv == CONV_COPY && unit == 16 && q.row_src_bytes <= kMaxStageBytes &&
-                       !(options & (PMG_OPT_FORCE_SIMT | PMG_OPT_FORCE_SCALAR));
+  const bool forced = (options & (PMG_OPT_FORCE_SIMT | PMG_OPT_FORCE_SCALAR)) != 0;
+  const bool bulk_ok = conv == CONV_COPY && unit == 16 && q.row_src_bytes <= kMaxStageBytes && !forced;
+  // converting TMA path: source rows fit 16-byte bulk copies, output units are
+  // 16-byte stores
+  const int cu_unit = tma_convert_unit(conv);
+  const bool tma_cvt_ok = conv != CONV_COPY && !forced && cu_unit > 0 && E % cu_unit == 0 &&
+                          q.row_src_bytes % 16 == 0 && q.row_src_bytes <= kMaxStageBytes && aligned(cache, 16) &&
+                          q.blk_stride_b % 16 == 0 && q.tok_stride_b % 16 == 0 && aligned(dst, 16) &&
+                          q.dst_stride_b % 16 == 0;
+  q.src_dense = q.tok_stride_b == q.row_src_bytes;
+  q.dst_dense = q.dst_stride_b == q.row_dst_bytes;
   if (bulk_ok) {
     out.path = PMG_PATH_BULK;
-    q.src_dense = q.tok_stride_b == q.row_src_bytes;
-    q.dst_dense = q.dst_stride_b == q.row_dst_bytes;
-    // ring stages of whole rows, about 32 KB each
+    // ring stages of whole rows
     const int32_t rows = std::max(1, bulk_stage_target_bytes() / q.row_src_bytes);
     q.rows_per_stage = rows;
     q.stage_bytes = rows * q.row_src_bytes;
     out.unit = 0;
   } else {
-    const int64_t unit_elems = (conv == CONV_COPY) ? unit / es : unit;
-    out.path = (unit_elems > 1) ? PMG_PATH_VECTOR : PMG_PATH_SCALAR;
-    const int64_t upr = (conv == CONV_COPY) ? static_cast<int64_t>(E) * es / unit : E / unit;
+    int64_t upr;
+    if (tma_cvt_ok) {
+      out.path = PMG_PATH_BULK;
+      out.unit = cu_unit;
+      upr = E / cu_unit;
+      const int32_t rows = std::max(1, cvt_stage_target_bytes() / q.row_src_bytes);
+      q.rows_per_stage = rows;
+      q.stage_bytes = rows * q.row_src_bytes;
+      q.dense = q.dst_dense;
+    } else {
+      const int64_t unit_elems = (conv == CONV_COPY) ? unit / es : unit;
+      out.path = (unit_elems > 1) ? PMG_PATH_VECTOR : PMG_PATH_SCALAR;
+      upr = (conv == CONV_COPY) ? static_cast<int64_t>(E) * es / unit : E / unit;
+      q.dense = q.src_dense && q.dst_dense;
+    }
     q.units_per_row = static_cast<int32_t>(upr);
-    q.dense = (q.tok_stride_b == q.row_src_bytes) && (q.dst_stride_b == q.row_dst_bytes);
     if (!q.dense) {
-      // the row split divides 32-bit unit indices inside one page
+      // the row split divides 32-bit unit indices inside one page or stage
       if (static_cast<uint64_t>(B) * static_cast<uint64_t>(upr) >= (1ull << 32)) return PMG_ERR_UNSUPPORTED;
       uint32_t l = 0;
       while ((1ull << l) < static_cast<uint64_t>(upr)) ++l;
@@ -979,6 +1395,23 @@ const KernelFn kAllSimt[] = {
     gather_simt_kernel<CONV_F16_F32, 2>,    gather_simt_kernel<CONV_F16_F32, 1>,
 };
 
+KernelFn tma_convert_kernel_for(int conv) {
+  switch (conv) {
+    case CONV_E4M3_BF16: return gather_tma_convert_kernel<CONV_E4M3_BF16, 8>;
+    case CONV_E4M3_F16: return gather_tma_convert_kernel<CONV_E4M3_F16, 8>;
+    case CONV_E4M3_F32: return gather_tma_convert_kernel<CONV_E4M3_F32, 4>;
+    case CONV_BF16_F32: return gather_tma_convert_kernel<CONV_BF16_F32, 4>;
+    case CONV_F16_F32: return gather_tma_convert_kernel<CONV_F16_F32, 4>;
+    default: return nullptr;
+  }
+}
+
+const KernelFn kAllTmaConvert[] = {
+    gather_tma_convert_kernel<CONV_E4M3_BF16, 8>, gather_tma_convert_kernel<CONV_E4M3_F16, 8>,
+    gather_tma_convert_kernel<CONV_E4M3_F32, 4>,  gather_tma_convert_kernel<CONV_BF16_F32, 4>,
+    gather_tma_convert_kernel<CONV_F16_F32, 4>,
+};
+
 // Raises a kernel's dynamic shared memory limit to what the device allows
 // per block beyond the kernel's own static shared memory.
 int allow_max_dyn_smem(KernelFn k, int optin) {
@@ -1004,12 +1437,39 @@ int device_setup(int* sm_count) {
     if (allow_max_dyn_smem(reinterpret_cast<KernelFn>(gather_bulk_kernel), optin) != PMG_OK) return PMG_ERR_CUDA;
     for (KernelFn k : kAllSimt)
       if (allow_max_dyn_smem(k, optin) != PMG_OK) return PMG_ERR_CUDA;
+    for (KernelFn k : kAllTmaConvert)
+      if (allow_max_dyn_smem(k, optin) != PMG_OK) return PMG_ERR_CUDA;
     g_sm_count[dev] = n;
     g_optin_smem[dev] = optin;
     g_attr_set[dev] = true;
   }
   *sm_count = g_sm_count[dev];
   return PMG_OK;
+}
+
+// Whether launches carry the programmatic-dependent-launch attribute
+// (PMG_PDL=0 turns it off). The kernels wait for the previous grid before
+// reading any input, so the attribute only hides launch latency.
+bool use_pdl() {
+  static const bool v = [] {
+    const char* e = std::getenv("PMG_PDL");
+    return !(e && e[0] == '0');
+  }();
+  return v;
+}
+
+cudaError_t launch(KernelFn k, int64_t grid, int threads, size_t smem, cudaStream_t stream, const Params& q) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(static_cast<unsigned>(threads));
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = use_pdl() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k, q);
 }
 
 size_t host_plan_bytes(int R) { return (static_cast<size_t>(3) * R + 2) * sizeof(int32_t); }
@@ -1049,13 +1509,22 @@ int launch_gather(const Plan& pl, cudaStream_t stream) {
   if (st != PMG_OK) return st;
   const Params& q = pl.prm;
   const int64_t max_by_rows = (static_cast<int64_t>(q.T) + kMinRowsPerCta - 1) / kMinRowsPerCta;
-  if (pl.path == PMG_PATH_BULK) {
+  if (pl.path == PMG_PATH_BULK && pl.conv == CONV_COPY) {
     const size_t smem = static_cast<size_t>(kBulkStages) * q.stage_bytes + host_plan_bytes(q.R);
     int per_sm = 0;
     if (ctas_per_sm(gather_bulk_kernel, kBulkThreads, smem, &per_sm) != PMG_OK) return PMG_ERR_CUDA;
     if (per_sm < 1) return PMG_ERR_UNSUPPORTED;
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(static_cast<int64_t>(per_sm) * sms, max_by_rows));
-    gather_bulk_kernel<<<static_cast<unsigned>(grid), kBulkThreads, smem, stream>>>(q);
+    if (launch(gather_bulk_kernel, grid, kBulkThreads, smem, stream, q) != cudaSuccess) return PMG_ERR_CUDA;
+  } else if (pl.path == PMG_PATH_BULK) {
+    KernelFn k = tma_convert_kernel_for(pl.conv);
+    if (k == nullptr) return PMG_ERR_UNSUPPORTED;
+    const size_t smem = static_cast<size_t>(kCvtStages) * q.stage_bytes + host_plan_bytes(q.R);
+    int per_sm = 0;
+    if (ctas_per_sm(k, kCvtThreads, smem, &per_sm) != PMG_OK) return PMG_ERR_CUDA;
+    if (per_sm < 1) return PMG_ERR_UNSUPPORTED;
+    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(static_cast<int64_t>(per_sm) * sms, max_by_rows));
+    if (launch(k, grid, kCvtThreads, smem, stream, q) != cudaSuccess) return PMG_ERR_CUDA;
   } else {
     KernelFn k = simt_kernel_for(pl.conv, pl.unit);
     if (k == nullptr) return PMG_ERR_UNSUPPORTED;
@@ -1064,7 +1533,7 @@ int launch_gather(const Plan& pl, cudaStream_t stream) {
     if (ctas_per_sm(k, kPlanThreads, smem, &per_sm) != PMG_OK) return PMG_ERR_CUDA;
     if (per_sm < 1) return PMG_ERR_UNSUPPORTED;
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(static_cast<int64_t>(per_sm) * sms, max_by_rows));
-    k<<<static_cast<unsigned>(grid), kPlanThreads, smem, stream>>>(q);
+    if (launch(k, grid, kPlanThreads, smem, stream, q) != cudaSuccess) return PMG_ERR_CUDA;
   }
   return cudaGetLastError() == cudaSuccess ? PMG_OK : PMG_ERR_CUDA;
 }
@@ -1077,11 +1546,12 @@ int pmg_gather_ex(const void* cache, int64_t cache_block_stride, int64_t cache_t
                   const int32_t* block_table, int64_t block_table_stride, const int32_t* cu_seq_lens,
                   const int32_t* seq_starts, int32_t num_reqs, int64_t total_tokens, int32_t block_size,
                   int32_t entry_size, int32_t src_dtype, int32_t dst_dtype, const float* scale, void* dst,
-                  int64_t dst_token_stride, int32_t* error_flag, void* stream, uint32_t options) {
+                  int64_t dst_token_stride, int32_t* error_flag, int32_t* workspace, void* stream,
+                  uint32_t options) {
   Plan pl;
   const int st = make_plan(cache, cache_block_stride, cache_token_stride, num_blocks, block_table, block_table_stride,
                            cu_seq_lens, seq_starts, num_reqs, total_tokens, block_size, entry_size, src_dtype,
-                           dst_dtype, scale, dst, dst_token_stride, error_flag, options, pl);
+                           dst_dtype, scale, dst, dst_token_stride, error_flag, workspace, options, pl);
   if (st != PMG_OK) return st;
   if (pl.path == PMG_PATH_NONE) return PMG_OK;
   return launch_gather(pl, static_cast<cudaStream_t>(stream));
@@ -1094,7 +1564,7 @@ int pmg_gather(const void* cache, int64_t cache_block_stride, int64_t cache_toke
                int64_t dst_token_stride, int32_t* error_flag, void* stream) {
   return pmg_gather_ex(cache, cache_block_stride, cache_token_stride, num_blocks, block_table, block_table_stride,
                        cu_seq_lens, seq_starts, num_reqs, total_tokens, block_size, entry_size, src_dtype, dst_dtype,
-                       scale, dst, dst_token_stride, error_flag, stream, 0u);
+                       scale, dst, dst_token_stride, error_flag, nullptr, stream, 0u);
 }
 
 int pmg_select_path(const void* cache, int64_t cache_block_stride, int64_t cache_token_stride, int64_t num_blocks,
@@ -1105,7 +1575,7 @@ int pmg_select_path(const void* cache, int64_t cache_block_stride, int64_t cache
   Plan pl;
   const int st = make_plan(cache, cache_block_stride, cache_token_stride, num_blocks, block_table, block_table_stride,
                            cu_seq_lens, nullptr, num_reqs, total_tokens, block_size, entry_size, src_dtype, dst_dtype,
-                           nullptr, dst, dst_token_stride, nullptr, options, pl);
+                           nullptr, dst, dst_token_stride, nullptr, nullptr, options, pl);
   if (st != PMG_OK) return st;
   if (path_out) *path_out = pl.path;
   if (unit_elems_out) {

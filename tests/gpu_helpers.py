@@ -40,7 +40,7 @@ class DeviceCase:
 
     def __init__(self, wl: Workload, dst_row_stride: Optional[int] = None, device: str = "cuda:0",
                  cu: Optional[np.ndarray] = None, seq_starts="wl", block_table: Optional[np.ndarray] = None,
-                 total_tokens: Optional[int] = None, with_scale: bool = True):
+                 total_tokens: Optional[int] = None, with_scale: bool = True, workspace: bool = False):
         self.wl = wl
         self.device = device
         ed = ELEM_BYTES[wl.dst_dtype]
@@ -58,6 +58,7 @@ class DeviceCase:
             self.seq_starts = None if seq_starts is None else torch.from_numpy(seq_starts).to(device)
         self.scale = torch.tensor([wl.scale], dtype=torch.float32, device=device) if with_scale else None
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        self.ws = binding.new_workspace(device) if workspace else None
         nbytes = self.T * self.rs * ed
         self.raw = torch.full((GUARD_BYTES * 2 + nbytes,), FILL, dtype=torch.uint8, device=device)
         body = self.raw[GUARD_BYTES:GUARD_BYTES + nbytes]
@@ -67,13 +68,15 @@ class DeviceCase:
 
     def run(self, options: int = 0, stream=None) -> None:
         binding.gather(self.cache, self.dst, self.block_table, self.cu, self.seq_starts, self.scale, self.err,
-                       num_reqs=self.wl.num_reqs, stream=stream, options=options)
+                       num_reqs=self.wl.num_reqs, stream=stream, options=options, workspace=self.ws)
 
     def result(self) -> Tuple[np.ndarray, int, bool]:
         """(dst bits [T, row_stride], flag, guards intact)."""
         torch.cuda.synchronize(self.device)
         raw = self.raw.cpu().numpy()
         guards_ok = bool(np.all(raw[:GUARD_BYTES] == FILL) and np.all(raw[-GUARD_BYTES:] == FILL))
+        if self.ws is not None:
+            assert int(self.ws.abs().sum().item()) == 0, f"workspace not reset: {self.ws.tolist()}"
         ed = ELEM_BYTES[self.wl.dst_dtype]
         body = raw[GUARD_BYTES:len(raw) - GUARD_BYTES].view(NP_BITS[ed]).reshape(self.T, self.rs)
         return body, int(self.err.item()), guards_ok

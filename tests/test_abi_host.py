@@ -44,7 +44,7 @@ def test_status_strings(cuda_lib):
 def _args(**over):
     # host stand-ins: the host half only looks at pointer values
     a = dict(cache=16 * 1024, cbs=64 * 576, cts=576, nb=8, bt=4096, bts=4, cu=8192, ss=0, R=2, T=100, B=64,
-             E=576, sdt=0, ddt=0, scale=0, dst=32 * 1024, dts=576, err=0, opt=0)
+             E=576, sdt=0, ddt=0, scale=0, dst=32 * 1024, dts=576, err=0, ws=0, opt=0)
     a.update(over)
     return a
 
@@ -52,7 +52,8 @@ def _args(**over):
 def _gather(L, a):
     return L.pmg_gather_ex(a["cache"] or None, a["cbs"], a["cts"], a["nb"], a["bt"] or None, a["bts"],
                            a["cu"] or None, a["ss"] or None, a["R"], a["T"], a["B"], a["E"], a["sdt"], a["ddt"],
-                           a["scale"] or None, a["dst"] or None, a["dts"], a["err"] or None, None, a["opt"])
+                           a["scale"] or None, a["dst"] or None, a["dts"], a["err"] or None, a["ws"] or None, None,
+                           a["opt"])
 
 
 def _path(L, a):
@@ -70,11 +71,12 @@ def _path(L, a):
     (dict(nb=-1), 2), (dict(opt=64), 2),
     (dict(R=binding.MAX_REQS + 1), 5),
     (dict(cache=16 * 1024 + 1), 4), (dict(dst=32 * 1024 + 1), 4), (dict(bt=4098), 4), (dict(ss=8194), 4),
+    (dict(ws=64 * 1024 + 8), 4),
 ])
 def test_host_validation_rejects(cuda_lib, over, status):
     assert _gather(cuda_lib, _args(**over)) == status
     st, _, _ = _path(cuda_lib, _args(**over))
-    if "ss" not in over:  # select_path takes no seq_starts
+    if "ss" not in over and "ws" not in over:  # select_path takes neither
         assert st == status
 
 
@@ -93,11 +95,15 @@ def test_nothing_to_do_launches_nothing(cuda_lib, over):
     (dict(cts=640, cbs=64 * 640), "bulk", 0),                             # padded rows, still 16-B aligned
     (dict(cts=577, cbs=64 * 577), "scalar", 1),                           # 1154-B row starts: one bf16 per access
     (dict(E=7, cts=7, cbs=64 * 7, dts=7), "scalar", 1),
-    (dict(sdt=3, ddt=0), "vector", 16),                                   # fp8 -> bf16, 16 codes per load
+    (dict(sdt=3, ddt=0), "bulk", 0),                                      # fp8 -> bf16: TMA in, converter warps out
+    (dict(sdt=3, ddt=0, opt=binding.OPT_FORCE_SIMT), "vector", 16),       # fp8 -> bf16 SIMT, 16 codes per load
     (dict(sdt=3, ddt=0, cts=577, cbs=64 * 577), "scalar", 1),
-    (dict(sdt=3, ddt=2, dst=32 * 1024 + 16), "vector", 16),               # fp32 out, 16-B aligned
+    (dict(sdt=3, ddt=0, cts=640, cbs=64 * 640, dts=600), "bulk", 0),      # padded rows on both sides
+    (dict(sdt=3, ddt=0, E=572, cts=572, cbs=64 * 572, dts=572), "vector", 4),  # 572 % 8 != 0: SIMT
+    (dict(sdt=3, ddt=2, dst=32 * 1024 + 16), "bulk", 0),                  # fp32 out, 16-B aligned
     (dict(sdt=3, ddt=2, dst=32 * 1024 + 4), "scalar", 1),                 # fp32 out, only 4-B aligned rows
-    (dict(sdt=0, ddt=2), "vector", 8),                                    # bf16 -> fp32
+    (dict(sdt=0, ddt=2), "bulk", 0),                                      # bf16 -> fp32
+    (dict(sdt=0, ddt=2, dts=578), "vector", 2),                           # bf16 -> fp32, 8-B aligned out rows
     (dict(sdt=2, ddt=2), "bulk", 0),                                      # fp32 copy
     (dict(sdt=4, ddt=4, E=5, cts=5, cbs=320, dts=5), "scalar", 1),       # u8 odd rows
     (dict(sdt=4, ddt=4, E=12, cts=12, cbs=768, dts=12), "vector", 4),     # u8 rows of 12 B: 4-byte units

@@ -32,8 +32,8 @@ def _lib(cuda_lib):
     return cuda_lib
 
 
-def _check(wl, options=0, dst_row_stride=None, expect_flag=0, **kw):
-    case = DeviceCase(wl, dst_row_stride=dst_row_stride, **kw)
+def _check(wl, options=0, dst_row_stride=None, expect_flag=0, workspace=False, **kw):
+    case = DeviceCase(wl, dst_row_stride=dst_row_stride, workspace=workspace, **kw)
     case.run(options=options)
     got, flag, guards = case.result()
     want, oflag = oracle_run(wl, dst_row_stride=dst_row_stride, **{k: v for k, v in kw.items()
@@ -50,9 +50,35 @@ def _check(wl, options=0, dst_row_stride=None, expect_flag=0, **kw):
 # benchmark times ------------------------------------------------------------
 
 @pytest.mark.parametrize("name", ["tiny", "60k", "300k", "skew8", "skew64_raw", "skew64_dequant"])
-def test_named_workloads_full_size(name):
+@pytest.mark.parametrize("workspace", [False, True])
+def test_named_workloads_full_size(name, workspace):
     wl = W.CONFIGS[name]()
-    _check(wl)
+    _check(wl, workspace=workspace)
+
+
+@pytest.mark.parametrize("name", ["60k", "skew8", "skew64_dequant"])
+def test_workspace_reuse_across_calls_and_graph_replays(name):
+    """A workspace serves back-to-back calls (each leaves it zeroed), also when
+    the calls are replayed from a CUDA graph."""
+    wl = W.CONFIGS[name]()
+    case = DeviceCase(wl, workspace=True)
+    for _ in range(5):
+        case.run()
+    want, _ = oracle_run(wl)
+    got, flag, guards = case.result()
+    assert guards and flag == 0
+    assert_same(got, want, wl.dst_dtype, wl.src_dtype != wl.dst_dtype)
+    case.dst_full.view(torch.uint8).fill_(0xA5)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        s = torch.cuda.current_stream()
+        for _ in range(3):
+            case.run(stream=s)
+    for _ in range(4):
+        g.replay()
+    got, flag, guards = case.result()
+    assert guards and flag == 0
+    assert_same(got, want, wl.dst_dtype, wl.src_dtype != wl.dst_dtype)
 
 
 @pytest.mark.parametrize("name", ["tiny", "60k", "skew8", "skew64_raw"])
@@ -88,8 +114,10 @@ def _small(seed, src, dst, B, E, row_stride=None, starts=True, R=6, maxlen=None,
 @pytest.mark.parametrize("src,dst", PAIRS)
 @pytest.mark.parametrize("B,E", [(1, 576), (16, 7), (64, 576), (128, 8), (16, 512), (64, 656), (3, 1)])
 def test_dtype_block_entry_matrix(src, dst, B, E):
-    wl = _small(hash((src, dst, B, E)) % 10000, src, dst, B, E)
+    seed = sum(map(ord, src + dst)) * 1000 + B * 10 + E
+    wl = _small(seed, src, dst, B, E)
     _check(wl)
+    _check(wl, workspace=True)
 
 
 @pytest.mark.parametrize("src,dst", PAIRS)
@@ -98,6 +126,7 @@ def test_padded_rows_both_sides(src, dst, options):
     """Cache rows padded to 640 elements, dst rows padded to 600."""
     wl = _small(7, src, dst, 64, 576, row_stride=640, R=5, maxlen=300)
     _check(wl, options=options, dst_row_stride=600)
+    _check(wl, options=options, dst_row_stride=600, workspace=True)
 
 
 @pytest.mark.parametrize("row_stride,dst_stride", [(577, None), (576, 579), (581, 583)])
