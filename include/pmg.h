@@ -154,6 +154,41 @@ int pmg_gather_ex(const void* cache, int64_t cache_block_stride, int64_t cache_t
                   uint32_t options);
 
 /*
+ * pmg_gather_noalloc — pmg_gather with the dynamic work split of
+ * pmg_gather_ex, for callers that cannot allocate device memory. The pages
+ * have no counterpart of this entry point.
+ *
+ * Who needs it: code that may not call cudaMalloc, such as a serving engine
+ * that reserves nearly all of HBM for its own KV-cache pool up front, code
+ * running inside a CUDA stream capture (an allocation is not a stream operation
+ * and cannot be captured), or a latency-bound path that cannot afford
+ * cudaMalloc's implicit device synchronisation.
+ *
+ * The arguments, their meaning and the results are those of pmg_gather; the
+ * caller still passes every input and output. Instead of a caller workspace,
+ * the scheduling counter lives in a 256-byte static device array inside the
+ * library, which every GPU that loads the library holds until the process
+ * exits. The call needs PMG_WORKSPACE_INTS of those ints whatever the input
+ * sizes; inputs beyond pmg_gather's own limits (num_reqs > PMG_MAX_REQS, ...)
+ * are rejected with the same statuses (PMG_ERR_UNSUPPORTED, PMG_ERR_ARG, ...).
+ * It calls no cudaMalloc, cudaFree or other allocating routine: before each
+ * launch it clears the counter with cudaMemsetAsync on `stream`.
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current and caches it; make that
+ * first call before any stream capture. Every call shares the one array: calls
+ * that overlap on the GPU (different streams, or several host threads) race on
+ * it and may produce wrong output; serialise them, or use pmg_gather_ex with a
+ * workspace per stream.
+ */
+int pmg_gather_noalloc(const void* cache, int64_t cache_block_stride, int64_t cache_token_stride,
+                       int64_t num_blocks, const int32_t* block_table, int64_t block_table_stride,
+                       const int32_t* cu_seq_lens, const int32_t* seq_starts, int32_t num_reqs,
+                       int64_t total_tokens, int32_t block_size, int32_t entry_size, int32_t src_dtype,
+                       int32_t dst_dtype, const float* scale, void* dst, int64_t dst_token_stride,
+                       int32_t* error_flag, void* stream);
+
+/*
  * pmg_select_path — host-only: validates the layout arguments of a gather the
  * way pmg_gather_ex does and reports the path and the elements moved per
  * access it would use. Makes no CUDA call. Pointers are only inspected for

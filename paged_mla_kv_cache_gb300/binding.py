@@ -73,6 +73,8 @@ def load_library() -> ctypes.CDLL:
         L.pmg_gather.argtypes = gather_args
         L.pmg_gather_ex.restype = ctypes.c_int
         L.pmg_gather_ex.argtypes = gather_args[:18] + [vp, vp, u32]
+        L.pmg_gather_noalloc.restype = ctypes.c_int
+        L.pmg_gather_noalloc.argtypes = gather_args
         L.pmg_select_path.restype = ctypes.c_int
         L.pmg_select_path.argtypes = [vp, i64, i64, i64, vp, i64, vp, i32, i64, i32, i32, i32, i32, vp, i64, u32,
                                       ctypes.POINTER(i32), ctypes.POINTER(i32)]
@@ -153,6 +155,25 @@ def gather(cache: torch.Tensor, dst: torch.Tensor, block_table: torch.Tensor, cu
         _stream_handle(stream), int(options))
     if st != PMG_OK:
         raise PmgError(st, "pmg_gather")
+
+
+def gather_noalloc(cache: torch.Tensor, dst: torch.Tensor, block_table: torch.Tensor, cu_seq_lens: torch.Tensor,
+                   seq_starts: Optional[torch.Tensor] = None, scale: Optional[torch.Tensor] = None,
+                   error_flag: Optional[torch.Tensor] = None, num_reqs: Optional[int] = None, stream=None) -> None:
+    """gather() for callers that cannot allocate device memory: the dynamic
+    work split runs on the library's own static scratch instead of a caller
+    workspace (pmg_gather_noalloc). Calls that overlap on the GPU must not use
+    it concurrently; make the first call on a device outside stream capture."""
+    src_code, dst_code = _layout(cache, dst)
+    if num_reqs is None:
+        num_reqs = cu_seq_lens.shape[0] - 1
+    st = load_library().pmg_gather_noalloc(
+        _ptr(cache), cache.stride(0), cache.stride(1), cache.shape[0],
+        _ptr(block_table), _table_width(block_table), _ptr(cu_seq_lens), _ptr(seq_starts), int(num_reqs),
+        dst.shape[0], cache.shape[1], cache.shape[2], src_code, dst_code, _ptr(scale),
+        _ptr(dst), dst.stride(0), _ptr(error_flag), _stream_handle(stream))
+    if st != PMG_OK:
+        raise PmgError(st, "pmg_gather_noalloc")
 
 
 def new_workspace(device) -> torch.Tensor:

@@ -1540,7 +1540,73 @@ int launch_gather(const Plan& pl, cudaStream_t stream) {
 
 }  // namespace
 
+// ---------------------------------------------------------------------------
+// Scratch for pmg_gather_noalloc.
+//
+// Some callers cannot call cudaMalloc: a serving engine that hands nearly all
+// of HBM to its own KV-cache pool up front and lets nothing else allocate, code
+// that runs between the begin and end of a CUDA stream capture (an allocation is
+// not a stream operation and breaks or escapes the capture), and latency-bound
+// paths where cudaMalloc's implicit device synchronisation is not acceptable.
+// For them the scheduling counter of the dynamic work split lives here: a
+// file-scope device array that every GPU which loads this library holds until
+// the process exits. Its size is fixed and small; the gather needs
+// PMG_WORKSPACE_INTS of its ints whatever the input sizes.
+// ---------------------------------------------------------------------------
+constexpr int kNoAllocScratchInts = 64;  // 256 bytes
+static_assert(PMG_WORKSPACE_INTS <= kNoAllocScratchInts, "the scheduling counter must fit the static scratch");
+static __device__ __align__(256) int32_t g_noalloc_scratch[kNoAllocScratchInts];
+
+namespace {
+
+int32_t* g_noalloc_ptr[kMaxDevices];
+bool g_noalloc_ready[kMaxDevices];
+
+// Device address of g_noalloc_scratch on the current device. In host code the
+// array's name is only a host-side stand-in, so the address is looked up once
+// per device (with that device current) and cached.
+int noalloc_scratch(int32_t** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PMG_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return PMG_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_noalloc_ready[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) return PMG_ERR_CUDA;
+    g_noalloc_ptr[dev] = static_cast<int32_t*>(ptr);
+    g_noalloc_ready[dev] = true;
+  }
+  *out = g_noalloc_ptr[dev];
+  return PMG_OK;
+}
+
+}  // namespace
+
 extern "C" {
+
+int pmg_gather_noalloc(const void* cache, int64_t cache_block_stride, int64_t cache_token_stride, int64_t num_blocks,
+                       const int32_t* block_table, int64_t block_table_stride, const int32_t* cu_seq_lens,
+                       const int32_t* seq_starts, int32_t num_reqs, int64_t total_tokens, int32_t block_size,
+                       int32_t entry_size, int32_t src_dtype, int32_t dst_dtype, const float* scale, void* dst,
+                       int64_t dst_token_stride, int32_t* error_flag, void* stream) {
+  // every check of pmg_gather first, on the host, with no CUDA call
+  Plan pl;
+  int st = make_plan(cache, cache_block_stride, cache_token_stride, num_blocks, block_table, block_table_stride,
+                     cu_seq_lens, seq_starts, num_reqs, total_tokens, block_size, entry_size, src_dtype, dst_dtype,
+                     scale, dst, dst_token_stride, error_flag, nullptr, 0u, pl);
+  if (st != PMG_OK) return st;
+  if (pl.path == PMG_PATH_NONE) return PMG_OK;
+  int32_t* scratch = nullptr;
+  st = noalloc_scratch(&scratch);
+  if (st != PMG_OK) return st;
+  // The array keeps whatever the last call left; the claim counter must start
+  // at zero, so clear it on this stream ahead of the launch.
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(scratch, 0, PMG_WORKSPACE_INTS * sizeof(int32_t), s) != cudaSuccess) return PMG_ERR_CUDA;
+  pl.prm.sched = scratch;
+  return launch_gather(pl, s);
+}
+
 
 int pmg_gather_ex(const void* cache, int64_t cache_block_stride, int64_t cache_token_stride, int64_t num_blocks,
                   const int32_t* block_table, int64_t block_table_stride, const int32_t* cu_seq_lens,
