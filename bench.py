@@ -54,6 +54,22 @@ def dist_env():
     return ws, rank, local
 
 
+def reduce_max(x: float, device) -> float:
+    """Max over ranks of a per-rank float (the timed region's length); the
+    tensor lives on `device` (cuda for NCCL, cpu for gloo)."""
+    if not torch.distributed.is_initialized() or torch.distributed.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_value(bytes_per_step: int, steps: int, max_ms: float, world: int) -> float:
+    """Whole-job GB/s: every rank moved bytes_per_step per step; the job took the
+    slowest rank's time."""
+    return world * bytes_per_step * steps / (max_ms * 1e-3) / 1e9
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -211,18 +227,14 @@ def run_ours(args, wl: W.Workload, ws: int, rank: int, local: int):
     if ws > 1:
         torch.distributed.barrier()
     clocks = sampler.stop()
-    ms = start.elapsed_time(end)
-    if ws > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = reduce_max(start.elapsed_time(end), dev)
     for r in reps:
         flag = int(r.err.item())
         if flag != 0:
             raise RuntimeError(f"gather reported data errors (flag {flag}) on valid inputs")
 
     ms_per_step = ms / args.steps
-    value = ws * alg_bytes * args.steps / (ms * 1e-3) / 1e9
+    value = weak_value(alg_bytes, args.steps, ms, ws)
     # the gather is the only kernel of a step: its average launch duration is
     # the timed region over the steps (inter-launch gaps included)
     per_launch_ms = ms_per_step
