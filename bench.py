@@ -43,7 +43,13 @@ from paged_mla_kv_cache_gb300 import workloads as W  # noqa: E402
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
 METRIC = "effective gather GB/s (read+write / device time) and % of GB300 HBM peak"
-PROFILE_FILE = os.path.join(ROOT, "profiles", "gather_bulk_single60k.md")
+# committed ncu summary of the dominant kernel per workload
+PROFILE_FILES = {
+    "60k": "gather_bulk_single60k.md",
+    "300k": "gather_bulk_single300k.md",
+    "skew8": "gather_tma_convert_skew8.md",
+    "skew64_dequant": "gather_tma_convert_skew64_dequant.md",
+}
 KERNEL_SRC = os.path.join(ROOT, "paged_mla_kv_cache_gb300", "csrc", "pmg_gather.cu")
 
 
@@ -80,11 +86,14 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def profiled_traffic():
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel source (else None)."""
+def profiled_traffic(config: str):
+    """DRAM bytes per launch from the committed ncu summary of this workload, if
+    it was taken on the current kernel source (else None)."""
+    name = PROFILE_FILES.get(config)
+    if name is None:
+        return None
     try:
-        text = open(PROFILE_FILE).read()
+        text = open(os.path.join(ROOT, "profiles", name)).read()
     except OSError:
         return None
     m_sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
@@ -298,7 +307,7 @@ def run_ours(args, wl: W.Workload, ws: int, rank: int, local: int):
             "peak": peak,
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
-            "traffic": profiled_traffic(),
+            "traffic": profiled_traffic(args.config),
             "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
             "per_launch_us": round(per_launch_ms * 1e3, 2),
         },

@@ -131,8 +131,9 @@ int pmg_gather(const void* cache, int64_t cache_block_stride, int64_t cache_toke
  * (workspace NULL and options 0 is exactly pmg_gather).
  *
  *  workspace  device int32 [PMG_WORKSPACE_INTS], 16-byte aligned, or NULL.
- *             With a workspace, the TMA paths hand out the second half of the
- *             output rows in small pieces through an atomic counter, so CTAs
+ *             With a workspace, the TMA paths split a quarter of the output
+ *             rows evenly up front and hand out the rest in small pieces
+ *             through an atomic counter, so CTAs
  *             whose memory traffic is served faster take more of the work
  *             (without one, every CTA gets one equal share). The caller zeroes
  *             it once before first use; every call that completes leaves it

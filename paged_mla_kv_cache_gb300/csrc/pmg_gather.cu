@@ -53,7 +53,7 @@ namespace {
 
 constexpr int kPlanThreads = 256;        // SIMT kernel / debug-plan CTA size
 constexpr int kBulkThreads = 128;        // bulk kernel CTA size
-constexpr int kBulkStages = 4;           // TMA ring depth per CTA
+constexpr int kMaxStages = 8;            // TMA ring depth per CTA: at most this many stages
 constexpr int kMaxStageBytes = 48 * 1024;
 constexpr int kUnroll = 4;               // SIMT units in flight per thread
 constexpr int kMinRowsPerCta = 8;
@@ -96,6 +96,7 @@ struct Params {
   int32_t upr_shift;
   int32_t dense;          // src and dst rows are back to back: no row split
   // bulk mover
+  int32_t stages;         // ring depth (<= kMaxStages)
   int32_t stage_bytes;    // bytes of one ring stage
   int32_t rows_per_stage;
   int32_t src_dense;
@@ -129,20 +130,6 @@ __device__ __forceinline__ int32_t ld_meta(const int32_t* ptr, uint64_t pol) {
   int32_t v;
   asm volatile("ld.global.nc.L2::cache_hint.b32 %0, [%1], %2;" : "=r"(v) : "l"(ptr), "l"(pol));
   return v;
-}
-
-// The CTAs of a launch together prefetch the whole block table into L2 at
-// entry, so the block-id reads that follow the plan hit L2 instead of waiting
-// on DRAM behind the plan's own reads. Skipped for tables above 4 MB.
-__device__ __forceinline__ void prefetch_block_table(const int32_t* bt, int64_t rows, int64_t stride) {
-  const int64_t bytes = rows * stride * static_cast<int64_t>(sizeof(int32_t));
-  if (bytes <= 0 || bytes > (4ll << 20)) return;
-  const uintptr_t first = reinterpret_cast<uintptr_t>(bt) & ~static_cast<uintptr_t>(127);
-  const uintptr_t last = (reinterpret_cast<uintptr_t>(bt) + static_cast<uintptr_t>(bytes) - 1) & ~static_cast<uintptr_t>(127);
-  const int64_t lines = static_cast<int64_t>((last - first) / 128) + 1;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < lines;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
-    asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(first + static_cast<uintptr_t>(i) * 128));
 }
 
 // Programmatic dependent launch: let the next kernel in the stream begin its
@@ -186,11 +173,11 @@ struct PlanView {
   int32_t* P;   // [R + 1] exclusive prefix of page counts
 };
 
-__device__ __forceinline__ PlanView plan_view(uint8_t* base, int R) {
+__device__ __forceinline__ PlanView plan_view(uint8_t* base, const Params& p) {
   PlanView v;
   v.ob = reinterpret_cast<int32_t*>(base);
-  v.st = v.ob + (R + 1);
-  v.P = v.st + R;
+  v.st = v.ob + (p.R + 1);
+  v.P = v.st + p.R;
   return v;
 }
 
@@ -207,22 +194,26 @@ __device__ __forceinline__ int32_t request_pages(const PlanView& v, int r, int B
   return static_cast<int32_t>(last - first + 1u);
 }
 
-// Builds the plan with all threads of the CTA. Returns the number of page
-// tasks, or -1 when cu_seq_lens is not non-decreasing from a non-negative
-// start (then nothing may be written). report_flags: this CTA reports the
-// plan-level flag bits (one CTA per launch does, to keep atomics rare).
+// Builds the plan. kWarp = false: all threads of the CTA take part (any R up
+// to PMG_MAX_REQS). kWarp = true: one warp builds it alone, with no CTA-wide
+// barrier, for R <= kWarpPlanMaxReqs. Returns the number of page tasks, or -1
+// when cu_seq_lens is not non-decreasing from a non-negative start (then
+// nothing may be written). report_flags: this CTA reports the plan-level flag
+// bits (one CTA per launch does, to keep atomics rare).
+constexpr int kWarpPlanMaxReqs = 256;
+
+template <bool kWarp>
 __device__ int build_plan(const Params& p, const PlanView& v, bool report_flags) {
   __shared__ int32_t warp_sums[32];
   __shared__ int32_t total_pages;
-  const int tid = threadIdx.x;
-  const int nt = blockDim.x;
+  const int tid = kWarp ? static_cast<int>(threadIdx.x & 31) : static_cast<int>(threadIdx.x);
+  const int nt = kWarp ? 32 : static_cast<int>(blockDim.x);
   const int R = p.R;
   const int64_t T = p.T;
 
   int bad = 0;
   int bad_start = 0;
   const uint64_t keep = evict_last_policy();
-  if (p.bt != nullptr) prefetch_block_table(p.bt, R, p.bt_stride);
   for (int r = tid; r <= R; r += nt) {
     int64_t c;
     if (p.implied_end && r == R) {
@@ -239,7 +230,8 @@ __device__ int build_plan(const Params& p, const PlanView& v, bool report_flags)
     v.ob[r] = static_cast<int32_t>(c < T ? c : T);
     if (r < R) v.st[r] = p.ss ? ld_meta(p.ss + r, keep) : 0;
   }
-  if (__syncthreads_or(bad)) {
+  const bool any_bad = kWarp ? (__syncwarp(), __any_sync(0xffffffffu, bad)) : __syncthreads_or(bad);
+  if (any_bad) {
     if (report_flags && tid == 0) set_flag(p, PMG_FLAG_CU_ORDER);
     return -1;
   }
@@ -254,35 +246,68 @@ __device__ int build_plan(const Params& p, const PlanView& v, bool report_flags)
     if (v.st[r] < 0 && v.ob[r + 1] > v.ob[r]) bad_start = 1;
   }
   const int lane = tid & 31;
-  const int warp = tid >> 5;
-  const int nwarps = (nt + 31) >> 5;
   int32_t x = local;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
     if (lane >= o) x += y;
   }
-  if (lane == 31) warp_sums[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    int32_t w = lane < nwarps ? warp_sums[lane] : 0;
+  int32_t base, total;
+  if (kWarp) {
+    total = __shfl_sync(0xffffffffu, x, 31);
+    base = x - local;
+  } else {
+    const int warp = tid >> 5;
+    const int nwarps = (nt + 31) >> 5;
+    if (lane == 31) warp_sums[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+      int32_t w = lane < nwarps ? warp_sums[lane] : 0;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int32_t y = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= o) w += y;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int32_t y = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += y;
+      }
+      if (lane < nwarps) warp_sums[lane] = w;
+      if (lane == nwarps - 1) total_pages = w;
     }
-    if (lane < nwarps) warp_sums[lane] = w;
-    if (lane == nwarps - 1) total_pages = w;
+    __syncthreads();
+    base = (warp > 0 ? warp_sums[warp - 1] : 0) + x - local;
+    total = total_pages;
   }
-  __syncthreads();
-  int32_t base = (warp > 0 ? warp_sums[warp - 1] : 0) + x - local;
   for (int r = rb; r < re; ++r) {
     v.P[r] = base;
     base += request_pages(v, r, p.B);
   }
-  if (tid == 0) v.P[R] = total_pages;
-  if (__syncthreads_or(bad_start) && report_flags && tid == 0) set_flag(p, PMG_FLAG_SEQ_START);
-  return total_pages;
+  if (tid == 0) v.P[R] = total;
+  const bool any_bad_start = kWarp ? (__syncwarp(), __any_sync(0xffffffffu, bad_start)) : __syncthreads_or(bad_start);
+  if (any_bad_start && report_flags && tid == 0) set_flag(p, PMG_FLAG_SEQ_START);
+  return total;
+}
+
+// Before the previous grid is known to be done, a kernel may not read its
+// inputs, but it may warm L2 with them: a prefetch is not a read into
+// registers, and L2 is the point of coherence for later loads. Every CTA
+// prefetches the lines of cu_seq_lens and seq_starts; the CTAs of the launch
+// share the block table (tables up to 4 MB).
+__device__ __forceinline__ void prefetch_lines(const void* ptr, int64_t bytes, int64_t first_idx, int64_t step) {
+  if (ptr == nullptr || bytes <= 0) return;
+  const uintptr_t first = reinterpret_cast<uintptr_t>(ptr) & ~static_cast<uintptr_t>(127);
+  const uintptr_t last = (reinterpret_cast<uintptr_t>(ptr) + static_cast<uintptr_t>(bytes) - 1) & ~static_cast<uintptr_t>(127);
+  const int64_t lines = static_cast<int64_t>((last - first) / 128) + 1;
+  for (int64_t i = first_idx; i < lines; i += step)
+    asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(first + static_cast<uintptr_t>(i) * 128));
+}
+
+__device__ __forceinline__ void prefetch_metadata(const Params& p) {
+  const int64_t R = p.R;
+  const int64_t cu_n = p.implied_end ? R : R + 1;
+  prefetch_lines(p.cu, cu_n * 4, threadIdx.x, blockDim.x);
+  prefetch_lines(p.ss, R * 4, threadIdx.x, blockDim.x);
+  const int64_t bt_bytes = R * p.bt_stride * 4;
+  if (bt_bytes <= (4ll << 20))
+    prefetch_lines(p.bt, bt_bytes, static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x,
+                   static_cast<int64_t>(gridDim.x) * blockDim.x);
 }
 
 struct PageTask {
@@ -445,12 +470,16 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 
 // Wait until at most n committed bulk-store groups still read shared memory.
 __device__ __forceinline__ void bulk_wait_read_upto(int n) {
-  static_assert(kBulkStages == 4, "update the cases below");
+  static_assert(kMaxStages == 8, "update the cases below");
   switch (n) {
     case 0: asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); break;
     case 1: asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); break;
     case 2: asm volatile("cp.async.bulk.wait_group.read 2;" ::: "memory"); break;
-    default: asm volatile("cp.async.bulk.wait_group.read 3;" ::: "memory"); break;
+    case 3: asm volatile("cp.async.bulk.wait_group.read 3;" ::: "memory"); break;
+    case 4: asm volatile("cp.async.bulk.wait_group.read 4;" ::: "memory"); break;
+    case 5: asm volatile("cp.async.bulk.wait_group.read 5;" ::: "memory"); break;
+    case 6: asm volatile("cp.async.bulk.wait_group.read 6;" ::: "memory"); break;
+    default: asm volatile("cp.async.bulk.wait_group.read 7;" ::: "memory"); break;
   }
 }
 
@@ -500,9 +529,10 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 // ---------------------------------------------------------------------------
 // Work items. Without a workspace, CTA c owns one balanced share of the output
 // rows (static). With a workspace, item c < G is CTA c's static first share (a
-// rows; half of all rows together) and items >= G (d rows each) are claimed in
-// order through an atomic counter, so CTAs that get their data faster take more
-// of the rest; the last CTA to finish resets the counter for the next call.
+// rows; a quarter of all rows together by default) and items >= G (d rows
+// each) are claimed in order through an atomic counter, so CTAs that get their
+// data faster take more of the rest; the CTA making a launch's last claim
+// resets the counter for the next call.
 // ---------------------------------------------------------------------------
 
 struct Items {
@@ -574,11 +604,16 @@ __device__ __forceinline__ void segq_init(SegQueue& q) {
 // The scheduler warp: takes items (its static one, then claimed ones) and
 // resolves each into batches of up to 32 segments, one task per lane (map,
 // block-table read, bounds checks). Returns false on a timeout.
-__device__ bool run_scheduler(const Params& p, const PlanView& v, int32_t num_tasks, const Items& its, SegQueue& q) {
+__device__ bool run_scheduler(const Params& p, const PlanView& v, int32_t num_tasks, SegQueue& q) {
   const int lane = threadIdx.x & 31;
   uint32_t uses = 0;
   uint32_t k = blockIdx.x;
-  bool have = k < its.n;
+  Items its{};
+  bool have = false;
+  if (num_tasks > 0) {
+    its = make_items(v, p);
+    have = k < its.n;
+  }
   while (have) {
     // claim the next item now; its latency overlaps this item's resolution
     uint32_t claimed = 0;
@@ -674,45 +709,52 @@ __device__ __forceinline__ void issue_loads(const Params& p, const Chunk& c, uin
   }
 }
 
-// Byte copy: warp 0 lane 0 loads chunks into a ring of kBulkStages stages and
+// Byte copy: warp 0 lane 0 loads chunks into a ring of p.stages stages (at most kMaxStages) and
 // stores each landed stage straight back out; warp 1 schedules.
 __global__ void __launch_bounds__(kBulkThreads) gather_bulk_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ __align__(8) uint64_t full_bar[kBulkStages];
-  __shared__ Chunk stage_chunk[kBulkStages];
+  __shared__ __align__(8) uint64_t full_bar[kMaxStages];
+  __shared__ Chunk stage_chunk[kMaxStages];
   __shared__ __align__(8) SegQueue q;
 
   // layout: [stages][plan]; stage buffers first keeps them 128-byte aligned
   uint8_t* stage_base = smem;
-  const PlanView v = plan_view(smem + static_cast<size_t>(kBulkStages) * p.stage_bytes, p.R);
-
-  pdl_entry();
-  const int32_t num_tasks = build_plan(p, v, blockIdx.x == 0);
-  if (num_tasks <= 0) return;
-  const Items its = make_items(v, p);
+  const PlanView v = plan_view(smem + static_cast<size_t>(p.stages) * p.stage_bytes, p);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
+  // nothing before the PDL wait reads an input: barrier set-up, L2 prefetch
   if (tid == 0) {
-    for (int s = 0; s < kBulkStages; ++s) mbar_init(&full_bar[s], 1);
+    for (int s = 0; s < p.stages; ++s) mbar_init(&full_bar[s], 1);
     segq_init(q);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
+  prefetch_metadata(p);
+  pdl_entry();
   __syncthreads();
+  // small batches: the scheduler warp plans alone; large ones: the whole CTA
+  const bool warp_plan = p.R <= kWarpPlanMaxReqs;
+  int32_t num_tasks = 0;
+  if (!warp_plan) {
+    num_tasks = build_plan<false>(p, v, blockIdx.x == 0);
+    if (num_tasks <= 0) return;
+  }
 
   if (warp == 1) {
-    if (!run_scheduler(p, v, num_tasks, its, q)) set_flag(p, PMG_FLAG_TIMEOUT);
+    if (warp_plan) num_tasks = build_plan<true>(p, v, blockIdx.x == 0);
+    if (!run_scheduler(p, v, num_tasks, q)) set_flag(p, PMG_FLAG_TIMEOUT);
   } else if (tid == 0) {
     const uint64_t pol = evict_first_policy();
     const uint32_t row_bytes = static_cast<uint32_t>(p.row_src_bytes);
+    const uint32_t S = static_cast<uint32_t>(p.stages);
     SegReader rd{0, -1, 0, ChunkIter{0, 0}, false};
     uint32_t loads = 0, stores = 0;
     bool gen_done = false;
     bool ok = true;
     for (;;) {
-      // keep up to kBulkStages chunks loading ahead of the stores
-      while (!gen_done && loads - stores < static_cast<uint32_t>(kBulkStages)) {
+      // keep up to p.stages chunks loading ahead of the stores
+      while (!gen_done && loads - stores < S) {
         Chunk c;
         const int r = rd.next(q, p, c, loads == stores);
         if (r == 0) break;
@@ -721,10 +763,10 @@ __global__ void __launch_bounds__(kBulkThreads) gather_bulk_kernel(const __grid_
           if (r == -2) ok = false;
           break;
         }
-        const int s = static_cast<int>(loads % kBulkStages);
-        if (loads >= static_cast<uint32_t>(kBulkStages)) {
+        const int s = static_cast<int>(loads % S);
+        if (loads >= S) {
           // the store that last used stage s must have finished reading it
-          bulk_wait_read_upto(static_cast<int>(stores - 1 - (loads - kBulkStages)));
+          bulk_wait_read_upto(static_cast<int>(stores - 1 - (loads - S)));
         }
         stage_chunk[s] = c;
         issue_loads(p, c, stage_base + static_cast<size_t>(s) * p.stage_bytes, &full_bar[s], pol);
@@ -734,8 +776,8 @@ __global__ void __launch_bounds__(kBulkThreads) gather_bulk_kernel(const __grid_
         if (gen_done) break;
         continue;
       }
-      const int s = static_cast<int>(stores % kBulkStages);
-      if (!mbar_wait_bounded(&full_bar[s], (stores / kBulkStages) & 1u)) {
+      const int s = static_cast<int>(stores % S);
+      if (!mbar_wait_bounded(&full_bar[s], (stores / S) & 1u)) {
         ok = false;
         break;
       }
@@ -755,7 +797,7 @@ __global__ void __launch_bounds__(kBulkThreads) gather_bulk_kernel(const __grid_
       // land, then stop
       set_flag(p, PMG_FLAG_TIMEOUT);
       for (uint32_t k = stores + 1; k < loads; ++k)
-        (void)mbar_wait_bounded(&full_bar[k % kBulkStages], (k / kBulkStages) & 1u);
+        (void)mbar_wait_bounded(&full_bar[k % S], (k / S) & 1u);
     }
     bulk_wait_all();
   }
@@ -907,9 +949,10 @@ __global__ void __launch_bounds__(kPlanThreads) gather_simt_kernel(const __grid_
   __shared__ int64_t unit_prefix[kPlanThreads + 1];
   __shared__ int64_t warp_units[kPlanThreads / 32];
 
-  const PlanView v = plan_view(smem, p.R);
+  const PlanView v = plan_view(smem, p);
+  prefetch_metadata(p);
   pdl_entry();
-  const int32_t num_tasks = build_plan(p, v, blockIdx.x == 0);
+  const int32_t num_tasks = build_plan<false>(p, v, blockIdx.x == 0);
   if (num_tasks <= 0) return;
   const CtaRange range = cta_range(v, p.R, p.B, num_tasks);
   if (range.row0 >= range.row1) return;
@@ -1001,7 +1044,6 @@ __global__ void __launch_bounds__(kPlanThreads) gather_simt_kernel(const __grid_
 
 constexpr int kCvtWarps = 4;                        // converter warps
 constexpr int kCvtThreads = 32 * (kCvtWarps + 2);   // + producer warp + scheduler warp
-constexpr int kCvtStages = 4;
 
 template <int BYTES>
 __device__ __forceinline__ void load_smem(const uint8_t* src, Raw<BYTES>& r) {
@@ -1020,23 +1062,19 @@ __global__ void __launch_bounds__(kCvtThreads) gather_tma_convert_kernel(const _
   constexpr int kOutBytes = N * ConvTraits<CONV>::ed;
   static_assert(kOutBytes == 16, "one 16-byte store per unit");
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ __align__(8) uint64_t full_bar[kCvtStages];
-  __shared__ __align__(8) uint64_t empty_bar[kCvtStages];
-  __shared__ Chunk stage_chunk[kCvtStages];
+  __shared__ __align__(8) uint64_t full_bar[kMaxStages];
+  __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
+  __shared__ Chunk stage_chunk[kMaxStages];
   __shared__ __align__(8) SegQueue q;
 
   uint8_t* stage_base = smem;
-  const PlanView v = plan_view(smem + static_cast<size_t>(kCvtStages) * p.stage_bytes, p.R);
-  pdl_entry();
-  const int32_t num_tasks = build_plan(p, v, blockIdx.x == 0);
-  if (num_tasks <= 0) return;
-  const Items its = make_items(v, p);
-
+  const PlanView v = plan_view(smem + static_cast<size_t>(p.stages) * p.stage_bytes, p);
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
+  // nothing before the PDL wait reads an input: barrier set-up, L2 prefetch
   if (tid == 0) {
-    for (int s = 0; s < kCvtStages; ++s) {
+    for (int s = 0; s < p.stages; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], kCvtWarps);
     }
@@ -1044,20 +1082,31 @@ __global__ void __launch_bounds__(kCvtThreads) gather_tma_convert_kernel(const _
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
+  prefetch_metadata(p);
+  pdl_entry();
   __syncthreads();
+  // small batches: the scheduler warp plans alone; large ones: the whole CTA
+  const bool warp_plan = p.R <= kWarpPlanMaxReqs;
+  int32_t num_tasks = 0;
+  if (!warp_plan) {
+    num_tasks = build_plan<false>(p, v, blockIdx.x == 0);
+    if (num_tasks <= 0) return;
+  }
 
   if (warp == kCvtWarps + 1) {
-    if (!run_scheduler(p, v, num_tasks, its, q)) set_flag(p, PMG_FLAG_TIMEOUT);
+    if (warp_plan) num_tasks = build_plan<true>(p, v, blockIdx.x == 0);
+    if (!run_scheduler(p, v, num_tasks, q)) set_flag(p, PMG_FLAG_TIMEOUT);
   } else if (warp == kCvtWarps) {
-    // producer: one lane issues the bulk loads, up to kCvtStages chunks ahead
+    // producer: one lane issues the bulk loads, up to p.stages chunks ahead
     if (lane == 0) {
       const uint64_t pol = evict_first_policy();
+      const uint32_t S = static_cast<uint32_t>(p.stages);
       SegReader rd{0, -1, 0, ChunkIter{0, 0}, false};
       for (uint32_t g = 0;; ++g) {
         Chunk c;
         const int r = rd.next(q, p, c, true);
-        const int s = static_cast<int>(g % kCvtStages);
-        const uint32_t use = g / kCvtStages;
+        const int s = static_cast<int>(g % S);
+        const uint32_t use = g / S;
         if (use > 0 && !mbar_wait_bounded(&empty_bar[s], (use - 1) & 1u)) {
           set_flag(p, PMG_FLAG_TIMEOUT);
           break;
@@ -1080,9 +1129,10 @@ __global__ void __launch_bounds__(kCvtThreads) gather_tma_convert_kernel(const _
       if (p.scale != nullptr) scale = __ldg(p.scale);
     }
     const uint32_t upr = static_cast<uint32_t>(p.units_per_row);
+    const uint32_t S = static_cast<uint32_t>(p.stages);
     for (uint32_t g = 0;; ++g) {
-      const int s = static_cast<int>(g % kCvtStages);
-      if (!mbar_wait_bounded(&full_bar[s], (g / kCvtStages) & 1u)) {
+      const int s = static_cast<int>(g % S);
+      if (!mbar_wait_bounded(&full_bar[s], (g / S) & 1u)) {
         set_flag(p, PMG_FLAG_TIMEOUT);
         break;
       }
@@ -1119,8 +1169,8 @@ __global__ void __launch_bounds__(kCvtThreads) gather_tma_convert_kernel(const _
 __global__ void __launch_bounds__(kPlanThreads) debug_plan_kernel(const __grid_constant__ Params p, int32_t* tasks_out,
                                                                   int64_t max_tasks, int64_t* num_tasks_out) {
   extern __shared__ __align__(128) uint8_t smem[];
-  const PlanView v = plan_view(smem, p.R);
-  const int32_t n = build_plan(p, v, true);
+  const PlanView v = plan_view(smem, p);
+  const int32_t n = build_plan<false>(p, v, true);
   const int32_t num = n < 0 ? 0 : n;
   if (threadIdx.x == 0) *num_tasks_out = num;
   const int64_t lim = num < max_tasks ? num : max_tasks;
@@ -1200,11 +1250,21 @@ int env_int(const char* name, int dflt, int lo, int hi) {
   return v < lo ? lo : (v > hi ? hi : v);
 }
 int sched_static_pct() {
-  static const int v = env_int("PMG_SCHED_STATIC_PCT", 50, 0, 100);
+  static const int v = env_int("PMG_SCHED_STATIC_PCT", 25, 0, 100);
   return v;
 }
 int sched_min_rows() {
   static const int v = env_int("PMG_SCHED_MIN_ROWS", 128, 1, 1 << 30);
+  return v;
+}
+
+// Ring depths (PMG_BULK_STAGES, PMG_CVT_STAGES: 2..8) for tuning sweeps.
+int bulk_stages() {
+  static const int v = env_int("PMG_BULK_STAGES", 4, 2, kMaxStages);
+  return v;
+}
+int cvt_stages() {
+  static const int v = env_int("PMG_CVT_STAGES", 4, 2, kMaxStages);
   return v;
 }
 
@@ -1329,6 +1389,7 @@ int make_plan(const void* cache, int64_t cbs, int64_t cts, int64_t num_blocks, c
     const int32_t rows = std::max(1, bulk_stage_target_bytes() / q.row_src_bytes);
     q.rows_per_stage = rows;
     q.stage_bytes = rows * q.row_src_bytes;
+    q.stages = bulk_stages();
     out.unit = 0;
   } else {
     int64_t upr;
@@ -1339,6 +1400,7 @@ int make_plan(const void* cache, int64_t cbs, int64_t cts, int64_t num_blocks, c
       const int32_t rows = std::max(1, cvt_stage_target_bytes() / q.row_src_bytes);
       q.rows_per_stage = rows;
       q.stage_bytes = rows * q.row_src_bytes;
+      q.stages = cvt_stages();
       q.dense = q.dst_dense;
     } else {
       const int64_t unit_elems = (conv == CONV_COPY) ? unit / es : unit;
@@ -1507,24 +1569,19 @@ int launch_gather(const Plan& pl, cudaStream_t stream) {
   int sms = 0;
   const int st = device_setup(&sms);
   if (st != PMG_OK) return st;
-  const Params& q = pl.prm;
+  Params q = pl.prm;
   const int64_t max_by_rows = (static_cast<int64_t>(q.T) + kMinRowsPerCta - 1) / kMinRowsPerCta;
-  if (pl.path == PMG_PATH_BULK && pl.conv == CONV_COPY) {
-    const size_t smem = static_cast<size_t>(kBulkStages) * q.stage_bytes + host_plan_bytes(q.R);
-    int per_sm = 0;
-    if (ctas_per_sm(gather_bulk_kernel, kBulkThreads, smem, &per_sm) != PMG_OK) return PMG_ERR_CUDA;
-    if (per_sm < 1) return PMG_ERR_UNSUPPORTED;
-    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(static_cast<int64_t>(per_sm) * sms, max_by_rows));
-    if (launch(gather_bulk_kernel, grid, kBulkThreads, smem, stream, q) != cudaSuccess) return PMG_ERR_CUDA;
-  } else if (pl.path == PMG_PATH_BULK) {
-    KernelFn k = tma_convert_kernel_for(pl.conv);
+  if (pl.path == PMG_PATH_BULK) {
+    const bool copy = pl.conv == CONV_COPY;
+    KernelFn k = copy ? gather_bulk_kernel : tma_convert_kernel_for(pl.conv);
     if (k == nullptr) return PMG_ERR_UNSUPPORTED;
-    const size_t smem = static_cast<size_t>(kCvtStages) * q.stage_bytes + host_plan_bytes(q.R);
+    const int threads = copy ? kBulkThreads : kCvtThreads;
+    const size_t smem = static_cast<size_t>(q.stages) * q.stage_bytes + host_plan_bytes(q.R);
     int per_sm = 0;
-    if (ctas_per_sm(k, kCvtThreads, smem, &per_sm) != PMG_OK) return PMG_ERR_CUDA;
+    if (ctas_per_sm(k, threads, smem, &per_sm) != PMG_OK) return PMG_ERR_CUDA;
     if (per_sm < 1) return PMG_ERR_UNSUPPORTED;
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(static_cast<int64_t>(per_sm) * sms, max_by_rows));
-    if (launch(k, grid, kCvtThreads, smem, stream, q) != cudaSuccess) return PMG_ERR_CUDA;
+    if (launch(k, grid, threads, smem, stream, q) != cudaSuccess) return PMG_ERR_CUDA;
   } else {
     KernelFn k = simt_kernel_for(pl.conv, pl.unit);
     if (k == nullptr) return PMG_ERR_UNSUPPORTED;
