@@ -48,30 +48,34 @@ def build(force: bool = False) -> str:
     return _LIB_PATH
 
 
+def load(path: str) -> ctypes.CDLL:
+    """Load an oracle library build and declare its C signatures."""
+    L = ctypes.CDLL(path)
+    i64, i32, vp = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p
+    L.pmg_oracle_gather.restype = ctypes.c_int
+    L.pmg_oracle_gather.argtypes = [
+        vp, i64, i64, i64, vp, i64, vp, vp, i32, i64, i32, i32,
+        ctypes.c_int, ctypes.c_int, ctypes.c_float, vp, i64]
+    L.pmg_oracle_e4m3_to_f32.restype = ctypes.c_float
+    L.pmg_oracle_e4m3_to_f32.argtypes = [ctypes.c_uint8]
+    L.pmg_oracle_bf16_to_f32.restype = ctypes.c_float
+    L.pmg_oracle_bf16_to_f32.argtypes = [ctypes.c_uint16]
+    L.pmg_oracle_f16_to_f32.restype = ctypes.c_float
+    L.pmg_oracle_f16_to_f32.argtypes = [ctypes.c_uint16]
+    L.pmg_oracle_f32_to_bf16.restype = ctypes.c_uint16
+    L.pmg_oracle_f32_to_bf16.argtypes = [ctypes.c_float]
+    L.pmg_oracle_f32_to_f16.restype = ctypes.c_uint16
+    L.pmg_oracle_f32_to_f16.argtypes = [ctypes.c_float]
+    L.pmg_oracle_pair_supported.restype = ctypes.c_int
+    L.pmg_oracle_pair_supported.argtypes = [ctypes.c_int, ctypes.c_int]
+    return L
+
+
 def lib() -> ctypes.CDLL:
     global _lib
     with _lock:
         if _lib is None:
-            path = build()
-            L = ctypes.CDLL(path)
-            i64, i32, vp = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p
-            L.pmg_oracle_gather.restype = ctypes.c_int
-            L.pmg_oracle_gather.argtypes = [
-                vp, i64, i64, i64, vp, i64, vp, vp, i32, i64, i32, i32,
-                ctypes.c_int, ctypes.c_int, ctypes.c_float, vp, i64]
-            L.pmg_oracle_e4m3_to_f32.restype = ctypes.c_float
-            L.pmg_oracle_e4m3_to_f32.argtypes = [ctypes.c_uint8]
-            L.pmg_oracle_bf16_to_f32.restype = ctypes.c_float
-            L.pmg_oracle_bf16_to_f32.argtypes = [ctypes.c_uint16]
-            L.pmg_oracle_f16_to_f32.restype = ctypes.c_float
-            L.pmg_oracle_f16_to_f32.argtypes = [ctypes.c_uint16]
-            L.pmg_oracle_f32_to_bf16.restype = ctypes.c_uint16
-            L.pmg_oracle_f32_to_bf16.argtypes = [ctypes.c_float]
-            L.pmg_oracle_f32_to_f16.restype = ctypes.c_uint16
-            L.pmg_oracle_f32_to_f16.argtypes = [ctypes.c_float]
-            L.pmg_oracle_pair_supported.restype = ctypes.c_int
-            L.pmg_oracle_pair_supported.argtypes = [ctypes.c_int, ctypes.c_int]
-            _lib = L
+            _lib = load(build())
     return _lib
 
 
