@@ -64,9 +64,15 @@ typedef enum pmg_status {
 #define PMG_FLAG_CU_ORDER 8      /* cu_seq_lens[0] < 0 or cu decreases: nothing written */
 #define PMG_FLAG_TIMEOUT 16      /* a bounded device wait ran out: output incomplete */
 
-/* Most requests one call accepts (the per-request page plan lives in shared
- * memory); larger batches return PMG_ERR_UNSUPPORTED. */
-#define PMG_MAX_REQS 4096
+/* Requests one launch plans in shared memory. A call with more requests needs
+ * a workspace (pmg_gather_ex, or pmg_gather_noalloc) and runs as a validation
+ * of the whole cu_seq_lens, one launch per group of PMG_MAX_REQS_PLAN
+ * requests, and a final one-thread launch; without a workspace it returns
+ * PMG_ERR_UNSUPPORTED. pmg_debug_plan is limited to this many. */
+#define PMG_MAX_REQS_PLAN 4096
+
+/* Most requests one call accepts; more return PMG_ERR_UNSUPPORTED. */
+#define PMG_MAX_REQS (1 << 20)
 
 /* Options of pmg_gather_ex. */
 #define PMG_OPT_FORCE_SIMT 1u      /* use the SIMT vector kernel even where TMA bulk applies */
@@ -100,7 +106,8 @@ typedef enum pmg_path {
  *                      non-decreasing from cu[0] >= 0 (else PMG_FLAG_CU_ORDER).
  *  seq_starts          int32 [num_reqs] or NULL (all zero): the first context
  *                      token of request r to copy.
- *  num_reqs            0 <= num_reqs <= PMG_MAX_REQS.
+ *  num_reqs            0 <= num_reqs <= PMG_MAX_REQS_PLAN (pmg_gather) or
+ *                      PMG_MAX_REQS (pmg_gather_ex with a workspace).
  *  total_tokens        T >= 0, rows of dst. Rows >= T are never written.
  *  block_size          tokens per block, >= 1.
  *  entry_size          elements per token entry, >= 1.

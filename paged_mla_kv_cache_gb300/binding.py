@@ -40,7 +40,8 @@ OPT_IMPLIED_END = 4
 
 PATH_NAMES = {0: "none", 1: "bulk", 2: "vector", 3: "scalar"}
 WORKSPACE_INTS = 4
-MAX_REQS = 4096
+MAX_REQS_PLAN = 4096       # requests one launch plans; more need a workspace
+MAX_REQS = 1 << 20         # requests one call accepts
 
 
 class PmgError(RuntimeError):

@@ -88,6 +88,7 @@ struct Params {
   const float* scale;     // may be null
   int32_t* err;           // may be null
   int32_t* sched;         // work-claim counter in the caller's workspace, or null (static split)
+  const int32_t* gate;    // large batches: non-zero when cu_seq_lens failed validation (write nothing)
   int32_t sched_static_pct;  // dynamic mode: share of rows split statically up front
   int32_t sched_min_rows;    // dynamic mode only when rows per CTA reach this
   // SIMT mover
@@ -195,7 +196,7 @@ __device__ __forceinline__ int32_t request_pages(const PlanView& v, int r, int B
 }
 
 // Builds the plan. kWarp = false: all threads of the CTA take part (any R up
-// to PMG_MAX_REQS). kWarp = true: one warp builds it alone, with no CTA-wide
+// to PMG_MAX_REQS_PLAN). kWarp = true: one warp builds it alone, with no CTA-wide
 // barrier, for R <= kWarpPlanMaxReqs. Returns the number of page tasks, or -1
 // when cu_seq_lens is not non-decreasing from a non-negative start (then
 // nothing may be written). report_flags: this CTA reports the plan-level flag
@@ -732,6 +733,7 @@ __global__ void __launch_bounds__(kBulkThreads) gather_bulk_kernel(const __grid_
   }
   prefetch_metadata(p);
   pdl_entry();
+  if (p.gate != nullptr && *reinterpret_cast<const volatile int32_t*>(p.gate) != 0) return;
   __syncthreads();
   // small batches: the scheduler warp plans alone; large ones: the whole CTA
   const bool warp_plan = p.R <= kWarpPlanMaxReqs;
@@ -952,6 +954,7 @@ __global__ void __launch_bounds__(kPlanThreads) gather_simt_kernel(const __grid_
   const PlanView v = plan_view(smem, p);
   prefetch_metadata(p);
   pdl_entry();
+  if (p.gate != nullptr && *reinterpret_cast<const volatile int32_t*>(p.gate) != 0) return;
   const int32_t num_tasks = build_plan<false>(p, v, blockIdx.x == 0);
   if (num_tasks <= 0) return;
   const CtaRange range = cta_range(v, p.R, p.B, num_tasks);
@@ -1084,6 +1087,7 @@ __global__ void __launch_bounds__(kCvtThreads) gather_tma_convert_kernel(const _
   }
   prefetch_metadata(p);
   pdl_entry();
+  if (p.gate != nullptr && *reinterpret_cast<const volatile int32_t*>(p.gate) != 0) return;
   __syncthreads();
   // small batches: the scheduler warp plans alone; large ones: the whole CTA
   const bool warp_plan = p.R <= kWarpPlanMaxReqs;
@@ -1160,6 +1164,35 @@ __global__ void __launch_bounds__(kCvtThreads) gather_tma_convert_kernel(const _
     }
   }
   __syncthreads();
+}
+
+// ---------------------------------------------------------------------------
+// Large batches (more requests than one launch plans in shared memory) run as
+// consecutive launches over groups of requests. cu_seq_lens is validated as a
+// whole first, so that an invalid array still writes nothing at all; the
+// verdict lives in the caller's workspace and is cleared by the last step.
+// ---------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(1024) validate_cu_kernel(const int32_t* cu, int32_t R, int32_t T, int32_t implied_end,
+                                                          int32_t* gate, int32_t* err) {
+  pdl_entry();
+  int bad = 0;
+  const int64_t n = implied_end ? R : static_cast<int64_t>(R) + 1;
+  for (int64_t r = threadIdx.x; r < n; r += blockDim.x) {
+    const int32_t c = cu[r];
+    if (r == 0 && c < 0) bad = 1;
+    if (r > 0 && c < cu[r - 1]) bad = 1;
+  }
+  (void)T;
+  if (__syncthreads_or(bad) && threadIdx.x == 0) {
+    *gate = 1;
+    if (err != nullptr) atomicOr(err, PMG_FLAG_CU_ORDER);
+  }
+}
+
+__global__ void clear_gate_kernel(int32_t* gate) {
+  pdl_entry();
+  if (threadIdx.x == 0) *gate = 0;
 }
 
 // ---------------------------------------------------------------------------
@@ -1313,6 +1346,9 @@ int make_plan(const void* cache, int64_t cbs, int64_t cts, int64_t num_blocks, c
     return PMG_ERR_ARG;
   if (options & ~(PMG_OPT_FORCE_SIMT | PMG_OPT_FORCE_SCALAR | PMG_OPT_IMPLIED_END)) return PMG_ERR_ARG;
   if (R > PMG_MAX_REQS) return PMG_ERR_UNSUPPORTED;
+  // more requests than one launch plans need the workspace (for the verdict
+  // of the whole-array validation)
+  if (R > PMG_MAX_REQS_PLAN && workspace == nullptr) return PMG_ERR_UNSUPPORTED;
   const int es = elem_bytes(sdt), ed = elem_bytes(ddt);
   if (static_cast<int64_t>(E) * ed > INT32_MAX || static_cast<int64_t>(E) * es > INT32_MAX) return PMG_ERR_UNSUPPORTED;
   if (R == 0 || T == 0) {
@@ -1565,7 +1601,7 @@ int ctas_per_sm(KernelFn k, int threads, size_t smem, int* out) {
   return PMG_OK;
 }
 
-int launch_gather(const Plan& pl, cudaStream_t stream) {
+int launch_one(const Plan& pl, cudaStream_t stream) {
   int sms = 0;
   const int st = device_setup(&sms);
   if (st != PMG_OK) return st;
@@ -1592,6 +1628,56 @@ int launch_gather(const Plan& pl, cudaStream_t stream) {
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(static_cast<int64_t>(per_sm) * sms, max_by_rows));
     if (launch(k, grid, kPlanThreads, smem, stream, q) != cudaSuccess) return PMG_ERR_CUDA;
   }
+  return cudaGetLastError() == cudaSuccess ? PMG_OK : PMG_ERR_CUDA;
+}
+
+// One call: a single launch, or, beyond PMG_MAX_REQS_PLAN requests, the
+// whole-array validation, one launch per group of requests (pointers into
+// cu_seq_lens, seq_starts and the block table advance by the group; output
+// rows come from the absolute cu values, so every group writes its own rows),
+// and the clearing of the verdict.
+int launch_gather(const Plan& pl, cudaStream_t stream) {
+  const Params& q = pl.prm;
+  if (q.R <= PMG_MAX_REQS_PLAN) return launch_one(pl, stream);
+  int sms = 0;
+  int st = device_setup(&sms);
+  if (st != PMG_OK) return st;
+  int32_t* gate = q.sched + 1;
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(1024);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = use_pdl() ? 1 : 0;
+    if (cudaLaunchKernelEx(&cfg, validate_cu_kernel, q.cu, q.R, q.T, q.implied_end, gate, q.err) != cudaSuccess)
+      return PMG_ERR_CUDA;
+  }
+  for (int64_t r0 = 0; r0 < q.R; r0 += PMG_MAX_REQS_PLAN) {
+    Plan g = pl;
+    const int32_t rg = static_cast<int32_t>(std::min<int64_t>(PMG_MAX_REQS_PLAN, q.R - r0));
+    g.prm.R = rg;
+    g.prm.cu = q.cu + r0;
+    g.prm.ss = q.ss ? q.ss + r0 : nullptr;
+    g.prm.bt = q.bt + r0 * q.bt_stride;
+    g.prm.implied_end = (q.implied_end && r0 + rg == q.R) ? 1 : 0;
+    g.prm.gate = gate;
+    st = launch_one(g, stream);
+    if (st != PMG_OK) return st;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(32);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = use_pdl() ? 1 : 0;
+  if (cudaLaunchKernelEx(&cfg, clear_gate_kernel, gate) != cudaSuccess) return PMG_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? PMG_OK : PMG_ERR_CUDA;
 }
 
@@ -1648,9 +1734,13 @@ int pmg_gather_noalloc(const void* cache, int64_t cache_block_stride, int64_t ca
                        int64_t dst_token_stride, int32_t* error_flag, void* stream) {
   // every check of pmg_gather first, on the host, with no CUDA call
   Plan pl;
+  // the static scratch stands in for the workspace (its address is only known
+  // after the CUDA set-up below; any 16-byte aligned non-null value passes the
+  // host checks)
+  int32_t* const placeholder = reinterpret_cast<int32_t*>(static_cast<uintptr_t>(256));
   int st = make_plan(cache, cache_block_stride, cache_token_stride, num_blocks, block_table, block_table_stride,
                      cu_seq_lens, seq_starts, num_reqs, total_tokens, block_size, entry_size, src_dtype, dst_dtype,
-                     scale, dst, dst_token_stride, error_flag, nullptr, 0u, pl);
+                     scale, dst, dst_token_stride, error_flag, placeholder, 0u, pl);
   if (st != PMG_OK) return st;
   if (pl.path == PMG_PATH_NONE) return PMG_OK;
   int32_t* scratch = nullptr;
@@ -1696,9 +1786,12 @@ int pmg_select_path(const void* cache, int64_t cache_block_stride, int64_t cache
                     int32_t dst_dtype, const void* dst, int64_t dst_token_stride, uint32_t options, int32_t* path_out,
                     int32_t* unit_elems_out) {
   Plan pl;
+  // the path does not depend on whether a workspace is given; a stand-in lets
+  // large batches through the host checks
+  int32_t* const placeholder = reinterpret_cast<int32_t*>(static_cast<uintptr_t>(256));
   const int st = make_plan(cache, cache_block_stride, cache_token_stride, num_blocks, block_table, block_table_stride,
                            cu_seq_lens, nullptr, num_reqs, total_tokens, block_size, entry_size, src_dtype, dst_dtype,
-                           nullptr, dst, dst_token_stride, nullptr, nullptr, options, pl);
+                           nullptr, dst, dst_token_stride, nullptr, placeholder, options, pl);
   if (st != PMG_OK) return st;
   if (path_out) *path_out = pl.path;
   if (unit_elems_out) {
@@ -1715,7 +1808,7 @@ int pmg_debug_plan(const int32_t* cu_seq_lens, const int32_t* seq_starts, int32_
                    int32_t* error_flag, void* stream, uint32_t options) {
   if (num_reqs < 0 || total_tokens < 0 || block_size < 1 || max_tasks < 0) return PMG_ERR_ARG;
   if (options & ~PMG_OPT_IMPLIED_END) return PMG_ERR_ARG;
-  if (num_reqs > PMG_MAX_REQS) return PMG_ERR_UNSUPPORTED;
+  if (num_reqs > PMG_MAX_REQS_PLAN) return PMG_ERR_UNSUPPORTED;
   if (num_tasks_out == nullptr || (num_reqs > 0 && cu_seq_lens == nullptr) || (max_tasks > 0 && tasks_out == nullptr))
     return PMG_ERR_NULL;
   Params q{};

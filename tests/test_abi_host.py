@@ -70,13 +70,15 @@ def _path(L, a):
     (dict(R=-1), 2), (dict(T=-1), 2), (dict(B=0), 2), (dict(E=0), 2), (dict(dts=575), 2), (dict(cts=-1), 2),
     (dict(nb=-1), 2), (dict(opt=64), 2),
     (dict(R=binding.MAX_REQS + 1), 5),
+    (dict(R=binding.MAX_REQS_PLAN + 1), 5),  # more than one launch plans needs a workspace
     (dict(cache=16 * 1024 + 1), 4), (dict(dst=32 * 1024 + 1), 4), (dict(bt=4098), 4), (dict(ss=8194), 4),
     (dict(ws=64 * 1024 + 8), 4),
 ])
 def test_host_validation_rejects(cuda_lib, over, status):
     assert _gather(cuda_lib, _args(**over)) == status
     st, _, _ = _path(cuda_lib, _args(**over))
-    if "ss" not in over and "ws" not in over:  # select_path takes neither
+    if "ss" not in over and "ws" not in over and over.get("R") != binding.MAX_REQS_PLAN + 1:
+        # select_path takes no seq_starts or workspace (and accepts large batches)
         assert st == status
 
 

@@ -153,7 +153,7 @@ def test_all_fp8_codes(scale, dst):
 
 def test_many_requests_at_the_limit():
     rng = np.random.default_rng(3)
-    R = binding.MAX_REQS
+    R = binding.MAX_REQS_PLAN
     lens = [int(x) for x in rng.integers(0, 40, R)]
     starts = [int(x) for x in rng.integers(0, 100, R)]
     wl = W.make_workload("many", lens, starts, 16, 64, None, "bf16", "bf16", 1.0, 5)
@@ -247,6 +247,58 @@ def test_invalid_cu_writes_nothing(cu):
 def test_huge_seq_start_no_overflow():
     wl = _flag_case()
     _check(wl, seq_starts=np.array([3, 2 ** 31 - 10, 7], np.int32), expect_flag=og.BAD_LOGICAL)
+
+
+# --- batches beyond one launch's plan: validated, then run in groups -----------
+
+def _large(R, seed, src="bf16", dst="bf16", E=64, B=16):
+    rng = np.random.default_rng(seed)
+    lens = [int(x) if rng.random() > 0.1 else 0 for x in rng.integers(0, 24, R)]
+    starts = [int(x) for x in rng.integers(0, 40, R)]
+    return W.make_workload("large", lens, starts, B, E, None, src, dst, 0.05, seed)
+
+
+@pytest.mark.parametrize("src,dst,options", [("bf16", "bf16", 0), ("fp8_e4m3", "bf16", 0),
+                                             ("bf16", "bf16", binding.OPT_FORCE_SIMT)])
+def test_large_batch_in_groups(src, dst, options):
+    wl = _large(2 * binding.MAX_REQS_PLAN + 1808, 61, src, dst)
+    _check(wl, options=options, workspace=True)
+
+
+def test_large_batch_needs_a_workspace():
+    wl = _large(binding.MAX_REQS_PLAN + 1, 62)
+    case = DeviceCase(wl)
+    with pytest.raises(binding.PmgError) as e:
+        case.run()
+    assert e.value.status == 5
+
+
+def test_large_batch_invalid_cu_in_last_group_writes_nothing():
+    wl = _large(2 * binding.MAX_REQS_PLAN + 100, 63)
+    cu = wl.cu_seq_lens.numpy().copy()
+    cu[-20] = cu[-21] - 1  # one decrease, in the last group only
+    _check(wl, cu=cu, expect_flag=og.BAD_CU, workspace=True)
+    # the verdict is cleared for the next call on the same workspace
+    case = DeviceCase(wl, workspace=True)
+    case.run()
+    case.run()
+    got, flag, guards = case.result()
+    want, _ = oracle_run(wl)
+    assert guards and flag == 0
+    assert_same(got, want, "bf16", False)
+
+
+def test_large_batch_implied_end():
+    wl = _large(binding.MAX_REQS_PLAN + 700, 64)
+    T = wl.total_tokens - 5
+    cu_short = wl.cu_seq_lens.numpy()[:-1].copy()
+    cu_full = np.concatenate([cu_short, [max(T, int(cu_short[-1]))]]).astype(np.int32)
+    want, oflag = oracle_run(wl, cu=cu_full, total_tokens=T)
+    case = DeviceCase(wl, cu=cu_short, total_tokens=T, workspace=True)
+    case.run(options=binding.OPT_IMPLIED_END)
+    got, flag, guards = case.result()
+    assert guards and oflag == 0 and flag == 0
+    assert_same(got, want, "bf16", False)
 
 
 # --- implied terminal entry (has_terminal_start = false) -----------------------

@@ -12,6 +12,7 @@ This file is collected last on purpose, so that a run stopping at the first
 failure has run every other test before it; it passes alone in a fresh process
 as well as after the rest.
 """
+import numpy as np
 import pytest
 import torch
 
@@ -49,6 +50,27 @@ def test_noalloc_matches_workspace_entry_point_twice(name):
         assert guards, f"call {call}: guard regions written"
         assert flag == 0, f"call {call}: flag {flag}"
         assert_same(got, want, wl.dst_dtype, wl.src_dtype != wl.dst_dtype)
+
+
+def test_noalloc_large_batch_matches_workspace_entry_point():
+    """More requests than one launch plans: the scratch also carries the verdict
+    of the whole-array cu_seq_lens check."""
+    rng = np.random.default_rng(65)
+    R = binding.MAX_REQS_PLAN + 900
+    lens = [int(x) for x in rng.integers(0, 20, R)]
+    wl = W.make_workload("large", lens, [int(x) for x in rng.integers(0, 30, R)], 16, 64, None, "bf16", "bf16",
+                         1.0, 65)
+    ref = DeviceCase(wl, workspace=True)
+    ref.run()
+    want, want_flag, _ = ref.result()
+    case = DeviceCase(wl)
+    for _ in range(2):
+        case.dst_full.view(torch.uint8).fill_(0xA5)
+        binding.gather_noalloc(case.cache, case.dst, case.block_table, case.cu, case.seq_starts, case.scale,
+                               case.err, num_reqs=wl.num_reqs)
+        got, flag, guards = case.result()
+        assert guards and flag == want_flag == 0
+        assert_same(got, want, "bf16", False)
 
 
 def test_noalloc_rejects_what_pmg_gather_rejects():
