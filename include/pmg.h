@@ -177,7 +177,7 @@ int pmg_gather_ex(const void* cache, int64_t cache_block_stride, int64_t cache_t
  * the scheduling counter lives in a 256-byte static device array inside the
  * library, which every GPU that loads the library holds until the process
  * exits. The call needs PMG_WORKSPACE_INTS of those ints whatever the input
- * sizes; inputs beyond pmg_gather's own limits (num_reqs > PMG_MAX_REQS, ...)
+ * sizes; inputs beyond pmg_gather_ex's limits (num_reqs > PMG_MAX_REQS, ...)
  * are rejected with the same statuses (PMG_ERR_UNSUPPORTED, PMG_ERR_ARG, ...).
  * It calls no cudaMalloc, cudaFree or other allocating routine: before each
  * launch it clears the counter with cudaMemsetAsync on `stream`.

@@ -31,6 +31,7 @@ BAD_LOGICAL = 1
 BAD_PHYS = 2
 BAD_START = 4
 BAD_CU = 8
+BAD_TOKEN = 32
 
 _lock = threading.Lock()
 _lib = None
@@ -68,6 +69,10 @@ def load(path: str) -> ctypes.CDLL:
     L.pmg_oracle_f32_to_f16.argtypes = [ctypes.c_float]
     L.pmg_oracle_pair_supported.restype = ctypes.c_int
     L.pmg_oracle_pair_supported.argtypes = [ctypes.c_int, ctypes.c_int]
+    L.pmg_oracle_gather_tokens.restype = ctypes.c_int
+    L.pmg_oracle_gather_tokens.argtypes = [
+        vp, i64, i64, i64, vp, i64, vp, vp, i32, i64, i32, i32,
+        ctypes.c_int, ctypes.c_int, ctypes.c_float, vp, i64]
     return L
 
 
@@ -111,6 +116,29 @@ def gather(cache: np.ndarray, block_table: np.ndarray, cu_seq_lens: np.ndarray,
         _ptr(bt), bt.shape[1], _ptr(cu), _ptr(ss), int(num_reqs), int(total_tokens),
         int(block_size), int(entry_size), DTYPE_CODES[src_dtype], DTYPE_CODES[dst_dtype],
         float(scale), _ptr(dst), dst.shape[1] if dst.size == 0 else dst.strides[0] // ed)
+    if rc < 0:
+        raise ValueError("oracle: call outside the defined domain (dtype pair or sizes)")
+    return rc
+
+
+def gather_tokens(cache: np.ndarray, block_table: np.ndarray, token_to_seq: np.ndarray, cu_seq_lens: np.ndarray,
+                  num_reqs: int, num_tokens: int, block_size: int, entry_size: int, src_dtype: str, dst_dtype: str,
+                  scale: float, dst: np.ndarray) -> int:
+    """The per-token indexed gather (output row t from request token_to_seq[t])
+    into ``dst`` (modified in place). Array conventions as in gather()."""
+    es, ed = ELEM_BYTES[src_dtype], ELEM_BYTES[dst_dtype]
+    assert cache.ndim == 3 and cache.itemsize == es and (cache.strides[2] == es or cache.size == 0)
+    assert dst.ndim == 2 and dst.itemsize == ed and (dst.strides[1] == ed or dst.size == 0)
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    t2s = np.ascontiguousarray(token_to_seq, dtype=np.int32)
+    cu = np.ascontiguousarray(cu_seq_lens, dtype=np.int32)
+    assert t2s.shape[0] >= num_tokens and cu.shape[0] >= num_reqs + 1
+    rc = lib().pmg_oracle_gather_tokens(
+        _ptr(cache), cache.shape[1] * cache.shape[2] if cache.size == 0 else cache.strides[0] // es,
+        cache.shape[2] if cache.size == 0 else cache.strides[1] // es, cache.shape[0],
+        _ptr(bt), bt.shape[1], _ptr(t2s), _ptr(cu), int(num_reqs), int(num_tokens), int(block_size),
+        int(entry_size), DTYPE_CODES[src_dtype], DTYPE_CODES[dst_dtype], float(scale), _ptr(dst),
+        dst.shape[1] if dst.size == 0 else dst.strides[0] // ed)
     if rc < 0:
         raise ValueError("oracle: call outside the defined domain (dtype pair or sizes)")
     return rc

@@ -45,7 +45,7 @@
 enum { O_BF16 = 0, O_FP16 = 1, O_FP32 = 2, O_E4M3 = 3, O_U8 = 4 };
 
 /* flag bits reported for invalid data */
-enum { O_BAD_LOGICAL = 1, O_BAD_PHYS = 2, O_BAD_START = 4, O_BAD_CU = 8 };
+enum { O_BAD_LOGICAL = 1, O_BAD_PHYS = 2, O_BAD_START = 4, O_BAD_CU = 8, O_BAD_TOKEN = 32 };
 
 static int elem_bytes(int dt) {
   switch (dt) {
@@ -236,6 +236,60 @@ int pmg_oracle_gather(const uint8_t* cache, int64_t cache_block_stride, int64_t 
       uint8_t* d = dst + (ob + i) * dst_token_stride * ed;
       for (int64_t e = 0; e < entry_size; ++e) convert_one(src + e * es, d + e * ed, src_dtype, dst_dtype, scale);
     }
+  }
+  return flag;
+}
+
+/*
+ * The per-token indexed gather of "indexer kernels take shape arguments at run
+ * time" (prhub.com.cn, vllm PR #56153), section "关键源码片段", the kernel
+ * _cp_gather_indexer_quant_cache_kernel: output token t
+ * belongs to request b = token_to_seq[t]; its context position is t minus the
+ * request's first output row cu_seq_lens[b]; the block table row b maps that
+ * position's logical block to a physical block. Every index is bounds-checked
+ * before use, the way that kernel masks its loads. A token whose request id is
+ * outside [0, num_reqs), or that lies outside its request's rows
+ * [cu[b], cu[b+1]), is skipped (bit 32); an out-of-row logical block (bit 1)
+ * or physical id (bit 2) skips the token too. Skipped output rows are left
+ * untouched. Returns the flag bits, or -1 outside the defined domain.
+ */
+int pmg_oracle_gather_tokens(const uint8_t* cache, int64_t cache_block_stride, int64_t cache_token_stride,
+                             int64_t num_blocks, const int32_t* block_table, int64_t block_table_stride,
+                             const int32_t* token_to_seq, const int32_t* cu_seq_lens, int32_t num_reqs,
+                             int64_t num_tokens, int32_t block_size, int32_t entry_size, int src_dtype, int dst_dtype,
+                             float scale, uint8_t* dst, int64_t dst_token_stride) {
+  if (!pmg_oracle_pair_supported(src_dtype, dst_dtype)) return -1;
+  if (num_reqs < 0 || num_tokens < 0 || block_size < 1 || entry_size < 1) return -1;
+  const int64_t es = elem_bytes(src_dtype);
+  const int64_t ed = elem_bytes(dst_dtype);
+  int flag = 0;
+  for (int64_t t = 0; t < num_tokens; ++t) {
+    const int64_t b = token_to_seq[t];
+    if (b < 0 || b >= num_reqs) {
+      flag |= O_BAD_TOKEN;
+      continue;
+    }
+    const int64_t first_row = cu_seq_lens[b];
+    const int64_t end_row = cu_seq_lens[b + 1];
+    if (t < first_row || t >= end_row) {
+      flag |= O_BAD_TOKEN;
+      continue;
+    }
+    const int64_t pos = t - first_row;
+    const int64_t lblock = pos / block_size;
+    const int64_t off = pos - lblock * block_size;
+    if (lblock >= block_table_stride) {
+      flag |= O_BAD_LOGICAL;
+      continue;
+    }
+    const int64_t pb = block_table[b * block_table_stride + lblock];
+    if (pb < 0 || pb >= num_blocks) {
+      flag |= O_BAD_PHYS;
+      continue;
+    }
+    const uint8_t* src = cache + (pb * cache_block_stride + off * cache_token_stride) * es;
+    uint8_t* row = dst + t * dst_token_stride * ed;
+    for (int64_t e = 0; e < entry_size; ++e) convert_one(src + e * es, row + e * ed, src_dtype, dst_dtype, scale);
   }
   return flag;
 }

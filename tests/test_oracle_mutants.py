@@ -41,6 +41,8 @@ MUTANTS = {
     "dequant scale dropped": ("v = pmg_oracle_e4m3_to_f32(s[0]) * scale;", "v = pmg_oracle_e4m3_to_f32(s[0]) * 1.0f;"),
     "cu order unchecked": ("if (cu_seq_lens[r + 1] < cu_seq_lens[r]) return O_BAD_CU;", ";"),
     "negative start accepted": ("if (len > 0 && start < 0) {", "if (len > 0 && start < -1000000) {"),
+    "token position off by one": ("const int64_t pos = t - first_row;", "const int64_t pos = t - first_row + 1;"),
+    "token row range unchecked": ("if (t < first_row || t >= end_row) {", "if (t >= end_row + 1000000) {"),
 }
 
 
@@ -180,7 +182,27 @@ def _pin_conversions():
     return _same(ours, ref, hnan)
 
 
-PINS = [_pin_hand_cases, _pin_library_route, _pin_padded_and_clamp, _pin_conversions]
+def _pin_token_cases():
+    for c in json.load(open(os.path.join(ROOT, "tests", "golden", "token_cases.json")))["cases"]:
+        E = 3
+        cache = _id_cache(c["num_blocks"], c["block_size"], E)
+        t2s = np.array(c["token_to_seq"], np.int32)
+        cu = np.array(c["cu_seq_lens"], np.int32)
+        dst = np.full((len(t2s), E), 0xA5A5A5A5, np.uint32)
+        flag = og.gather_tokens(cache, np.array(c["block_table"], np.int32), t2s, cu, len(cu) - 1, len(t2s),
+                                c["block_size"], E, "fp32", "fp32", 1.0, dst)
+        if flag != c["flag"]:
+            return False
+        for i, want in enumerate(c["rows"]):
+            if want is None:
+                if not np.all(dst[i] == 0xA5A5A5A5):
+                    return False
+            elif not np.array_equal(dst[i], cache[want[0], want[1]]):
+                return False
+    return True
+
+
+PINS = [_pin_hand_cases, _pin_library_route, _pin_padded_and_clamp, _pin_conversions, _pin_token_cases]
 
 
 def _run(pin) -> bool:
