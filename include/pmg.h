@@ -63,6 +63,7 @@ typedef enum pmg_status {
 #define PMG_FLAG_SEQ_START 4     /* seq_starts[r] < 0 with len_r > 0: request skipped */
 #define PMG_FLAG_CU_ORDER 8      /* cu_seq_lens[0] < 0 or cu decreases: nothing written */
 #define PMG_FLAG_TIMEOUT 16      /* a bounded device wait ran out: output incomplete */
+#define PMG_FLAG_TOKEN 32        /* pmg_gather_tokens: request id or row range of a token invalid: token skipped */
 
 /* Requests one launch plans in shared memory. A call with more requests needs
  * a workspace (pmg_gather_ex, or pmg_gather_noalloc) and runs as a validation
@@ -195,6 +196,32 @@ int pmg_gather_noalloc(const void* cache, int64_t cache_block_stride, int64_t ca
                        int64_t total_tokens, int32_t block_size, int32_t entry_size, int32_t src_dtype,
                        int32_t dst_dtype, const float* scale, void* dst, int64_t dst_token_stride,
                        int32_t* error_flag, void* stream);
+
+/*
+ * pmg_gather_tokens — per-token indexed gather, the gather pattern of the
+ * indexer kernel on the page "indexer kernels take shape arguments at run
+ * time" (prhub.com.cn, vllm PR #56153, section "关键源码片段":
+ * _cp_gather_indexer_quant_cache_kernel). Instead of deriving each output
+ * row's request from cu_seq_lens, the caller names it:
+ *
+ *  token_to_seq   int32 [num_tokens], device: request of output row t.
+ *  cu_seq_lens    int32 [num_reqs + 1], device: request b owns output rows
+ *                 [cu[b], cu[b+1]); row t reads context position t - cu[b].
+ *  num_tokens     rows of dst to produce, 0 <= num_tokens <= INT32_MAX.
+ *  options        0 or PMG_OPT_FORCE_SCALAR.
+ * Every other argument is as in pmg_gather (there is no seq_starts). Output
+ * row t = convert(cache[block_table[b, p / block_size], p % block_size]) with
+ * b = token_to_seq[t], p = t - cu[b]. Every index is checked before use: a
+ * request id outside [0, num_reqs) or a row outside [cu[b], cu[b+1]) skips the
+ * row (PMG_FLAG_TOKEN), a column past the block-table row or a block id outside
+ * [0, num_blocks) skips it too (PMG_FLAG_LOGICAL_BLOCK, PMG_FLAG_PHYS_BLOCK).
+ * Skipped rows are left untouched. Shapes are runtime arguments only.
+ */
+int pmg_gather_tokens(const void* cache, int64_t cache_block_stride, int64_t cache_token_stride, int64_t num_blocks,
+                      const int32_t* block_table, int64_t block_table_stride, const int32_t* token_to_seq,
+                      const int32_t* cu_seq_lens, int32_t num_reqs, int64_t num_tokens, int32_t block_size,
+                      int32_t entry_size, int32_t src_dtype, int32_t dst_dtype, const float* scale, void* dst,
+                      int64_t dst_token_stride, int32_t* error_flag, void* stream, uint32_t options);
 
 /*
  * pmg_select_path — host-only: validates the layout arguments of a gather the

@@ -33,6 +33,7 @@ FLAG_PHYS_BLOCK = 2
 FLAG_SEQ_START = 4
 FLAG_CU_ORDER = 8
 FLAG_TIMEOUT = 16
+FLAG_TOKEN = 32
 
 OPT_FORCE_SIMT = 1
 OPT_FORCE_SCALAR = 2
@@ -76,6 +77,9 @@ def load_library() -> ctypes.CDLL:
         L.pmg_gather_ex.argtypes = gather_args[:18] + [vp, vp, u32]
         L.pmg_gather_noalloc.restype = ctypes.c_int
         L.pmg_gather_noalloc.argtypes = gather_args
+        L.pmg_gather_tokens.restype = ctypes.c_int
+        L.pmg_gather_tokens.argtypes = [vp, i64, i64, i64, vp, i64, vp, vp, i32, i64, i32, i32, i32, i32, vp, vp, i64,
+                                        vp, vp, u32]
         L.pmg_select_path.restype = ctypes.c_int
         L.pmg_select_path.argtypes = [vp, i64, i64, i64, vp, i64, vp, i32, i64, i32, i32, i32, i32, vp, i64, u32,
                                       ctypes.POINTER(i32), ctypes.POINTER(i32)]
@@ -175,6 +179,25 @@ def gather_noalloc(cache: torch.Tensor, dst: torch.Tensor, block_table: torch.Te
         _ptr(dst), dst.stride(0), _ptr(error_flag), _stream_handle(stream))
     if st != PMG_OK:
         raise PmgError(st, "pmg_gather_noalloc")
+
+
+def gather_tokens(cache: torch.Tensor, dst: torch.Tensor, block_table: torch.Tensor, token_to_seq: torch.Tensor,
+                  cu_seq_lens: torch.Tensor, scale: Optional[torch.Tensor] = None,
+                  error_flag: Optional[torch.Tensor] = None, num_reqs: Optional[int] = None, stream=None,
+                  options: int = 0) -> None:
+    """Per-token indexed gather (pmg_gather_tokens): dst row t comes from
+    request token_to_seq[t] at position t - cu_seq_lens[token_to_seq[t]].
+    dst has num_tokens = len(token_to_seq) rows used."""
+    src_code, dst_code = _layout(cache, dst)
+    if num_reqs is None:
+        num_reqs = cu_seq_lens.shape[0] - 1
+    st = load_library().pmg_gather_tokens(
+        _ptr(cache), cache.stride(0), cache.stride(1), cache.shape[0],
+        _ptr(block_table), _table_width(block_table), _ptr(token_to_seq), _ptr(cu_seq_lens), int(num_reqs),
+        token_to_seq.shape[0], cache.shape[1], cache.shape[2], src_code, dst_code, _ptr(scale),
+        _ptr(dst), dst.stride(0), _ptr(error_flag), _stream_handle(stream), int(options))
+    if st != PMG_OK:
+        raise PmgError(st, "pmg_gather_tokens")
 
 
 def new_workspace(device) -> torch.Tensor:

@@ -1167,6 +1167,119 @@ __global__ void __launch_bounds__(kCvtThreads) gather_tma_convert_kernel(const _
 }
 
 // ---------------------------------------------------------------------------
+// Per-token indexed gather ("indexer kernels take shape arguments at run time",
+// vllm PR #56153, section "关键源码片段": _cp_gather_indexer_quant_cache_kernel).
+// Output row t reads request b = token_to_seq[t] at context position
+// t - cu_seq_lens[b]. One warp takes 32 consecutive tokens: each lane resolves
+// its token (request id, row range, block-table column, block id, all masked),
+// then the warp moves the 32 rows as a flat run of vector units, each lane
+// fetching the row base of its unit from the owning lane by shuffle.
+// ---------------------------------------------------------------------------
+
+struct TokParams {
+  const uint8_t* cache;
+  int64_t blk_stride_b;
+  int64_t tok_stride_b;
+  int64_t num_blocks;
+  const int32_t* bt;
+  int64_t bt_stride;
+  const int32_t* t2s;
+  const int32_t* cu;
+  int64_t T;  // num_tokens (<= INT32_MAX)
+  int32_t R;
+  int32_t B;
+  uint8_t* dst;
+  int64_t dst_stride_b;
+  const float* scale;
+  int32_t* err;
+  int32_t units_per_row;
+  uint32_t upr_magic;
+  int32_t upr_shift;
+};
+
+constexpr int kTokThreads = 256;
+
+template <int CONV, int N>
+__global__ void __launch_bounds__(kTokThreads) gather_tokens_kernel(const __grid_constant__ TokParams p) {
+  constexpr int kInBytes = N * ConvTraits<CONV>::es;
+  constexpr int kOutBytes = N * ConvTraits<CONV>::ed;
+  pdl_entry();
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (kTokThreads / 32);
+  float scale = 1.0f;
+  if (CONV == CONV_E4M3_BF16 || CONV == CONV_E4M3_F16 || CONV == CONV_E4M3_F32) {
+    if (p.scale != nullptr) scale = __ldg(p.scale);
+  }
+  const uint64_t keep = evict_last_policy();
+  const uint32_t upr = static_cast<uint32_t>(p.units_per_row);
+  int bits = 0;
+  for (int64_t tile = static_cast<int64_t>(blockIdx.x) * (kTokThreads / 32) + (threadIdx.x >> 5); tile * 32 < p.T;
+       tile += warps) {
+    const int64_t t = tile * 32 + lane;
+    int64_t src = -1;
+    if (t < p.T) {
+      const int32_t b = __ldg(p.t2s + t);
+      if (b < 0 || b >= p.R) {
+        bits |= PMG_FLAG_TOKEN;
+      } else {
+        const int64_t c0 = ld_meta(p.cu + b, keep);
+        const int64_t c1 = ld_meta(p.cu + b + 1, keep);
+        if (t < c0 || t >= c1) {
+          bits |= PMG_FLAG_TOKEN;
+        } else {
+          const uint32_t pos = static_cast<uint32_t>(t - c0);
+          const uint32_t lb = pos / static_cast<uint32_t>(p.B);
+          const uint32_t off = pos - lb * static_cast<uint32_t>(p.B);
+          if (static_cast<int64_t>(lb) >= p.bt_stride) {
+            bits |= PMG_FLAG_LOGICAL_BLOCK;
+          } else {
+            const int64_t phys = ld_meta(p.bt + static_cast<int64_t>(b) * p.bt_stride + lb, keep);
+            if (phys < 0 || phys >= p.num_blocks) {
+              bits |= PMG_FLAG_PHYS_BLOCK;
+            } else {
+              src = phys * p.blk_stride_b + static_cast<int64_t>(off) * p.tok_stride_b;
+            }
+          }
+        }
+      }
+    }
+    const int64_t dst_row = t * p.dst_stride_b;
+    const int64_t left = p.T - tile * 32;
+    const uint32_t nrows = static_cast<uint32_t>(left < 32 ? left : 32);
+    const uint32_t total = nrows * upr;
+    for (uint32_t base = 0; base < total; base += 32u * kUnroll) {
+      Raw<kInBytes> in[kUnroll];
+      int64_t dofs[kUnroll];
+      bool ok[kUnroll];
+#pragma unroll
+      for (int k = 0; k < kUnroll; ++k) {
+        const uint32_t u = base + static_cast<uint32_t>(k) * 32u + lane;
+        const uint32_t row = u < total ? fast_div(u, p.upr_magic, p.upr_shift) : 0u;
+        const int64_t s = __shfl_sync(0xffffffffu, src, static_cast<int>(row));
+        const int64_t d = __shfl_sync(0xffffffffu, dst_row, static_cast<int>(row));
+        ok[k] = u < total && s >= 0;
+        dofs[k] = 0;
+        if (ok[k]) {
+          const uint32_t col = u - row * upr;
+          load_raw<kInBytes>(p.cache + s + static_cast<int64_t>(col) * kInBytes, in[k]);
+          dofs[k] = d + static_cast<int64_t>(col) * kOutBytes;
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < kUnroll; ++k) {
+        if (ok[k]) {
+          Raw<kOutBytes> out;
+          convert_unit<CONV, N>(in[k], out, scale);
+          store_raw<kOutBytes>(p.dst + dofs[k], out);
+        }
+      }
+    }
+  }
+  bits = __reduce_or_sync(0xffffffffu, bits);
+  if (lane == 0 && bits != 0 && p.err != nullptr) atomicOr(p.err, bits);
+}
+
+// ---------------------------------------------------------------------------
 // Large batches (more requests than one launch plans in shared memory) run as
 // consecutive launches over groups of requests. cu_seq_lens is validated as a
 // whole first, so that an invalid array still writes nothing at all; the
@@ -1315,6 +1428,28 @@ int tma_convert_unit(int conv) {
 
 bool aligned(const void* ptr, int64_t a) { return (reinterpret_cast<uintptr_t>(ptr) % static_cast<uint64_t>(a)) == 0; }
 
+int unit_candidates(int conv, int* out);
+
+// Largest access unit (elements; bytes for a byte copy) that every source row
+// start, row length and destination row start allow.
+int pick_unit(int conv, int es, int ed, int32_t E, const void* cache, int64_t blk_b, int64_t tok_b, const void* dst,
+              int64_t dst_b) {
+  int cand[5];
+  const int ncand = unit_candidates(conv, cand);
+  for (int i = 0; i < ncand; ++i) {
+    const int n = cand[i];
+    const int64_t row_units_base = (conv == CONV_COPY) ? static_cast<int64_t>(E) * es : E;
+    const int64_t in_b = (conv == CONV_COPY) ? n : static_cast<int64_t>(n) * es;
+    const int64_t out_b = (conv == CONV_COPY) ? n : static_cast<int64_t>(n) * ed;
+    const int64_t out_align = out_b > 16 ? 16 : out_b;
+    if (row_units_base % n != 0) continue;
+    if (!aligned(cache, in_b) || blk_b % in_b != 0 || tok_b % in_b != 0) continue;
+    if (!aligned(dst, out_align) || dst_b % out_align != 0) continue;
+    return n;
+  }
+  return 1;
+}
+
 struct Plan {
   int path;         // pmg_path
   int conv;
@@ -1388,23 +1523,7 @@ int make_plan(const void* cache, int64_t cbs, int64_t cts, int64_t num_blocks, c
   q.sched_min_rows = sched_min_rows();
   out.conv = conv;
 
-  // largest access unit every row start and row length allows
-  int cand[5];
-  const int ncand = unit_candidates(conv, cand);
-  int unit = 1;
-  for (int i = 0; i < ncand; ++i) {
-    const int n = cand[i];
-    // for a byte copy the unit counts bytes of the row
-    const int64_t row_units_base = (conv == CONV_COPY) ? static_cast<int64_t>(E) * es : E;
-    const int64_t in_b = (conv == CONV_COPY) ? n : static_cast<int64_t>(n) * es;
-    const int64_t out_b = (conv == CONV_COPY) ? n : static_cast<int64_t>(n) * ed;
-    const int64_t out_align = out_b > 16 ? 16 : out_b;
-    if (row_units_base % n != 0) continue;
-    if (!aligned(cache, in_b) || q.blk_stride_b % in_b != 0 || q.tok_stride_b % in_b != 0) continue;
-    if (!aligned(dst, out_align) || q.dst_stride_b % out_align != 0) continue;
-    unit = n;
-    break;
-  }
+  int unit = pick_unit(conv, es, ed, E, cache, q.blk_stride_b, q.tok_stride_b, dst, q.dst_stride_b);
   if (options & PMG_OPT_FORCE_SCALAR) unit = (conv == CONV_COPY) ? es : 1;
   out.unit = unit;
 
@@ -1480,6 +1599,22 @@ KernelFn simt_kernel_for(int conv, int unit) {
   PMG_CASE(CONV_BF16_F32, 8) PMG_CASE(CONV_BF16_F32, 2) PMG_CASE(CONV_BF16_F32, 1)
   PMG_CASE(CONV_F16_F32, 8) PMG_CASE(CONV_F16_F32, 2) PMG_CASE(CONV_F16_F32, 1)
 #undef PMG_CASE
+  return nullptr;
+}
+
+using TokKernelFn = void (*)(TokParams);
+
+TokKernelFn tokens_kernel_for(int conv, int unit) {
+#define PMG_TCASE(C, N) \
+  if (conv == C && unit == N) return gather_tokens_kernel<C, N>;
+  PMG_TCASE(CONV_COPY, 16) PMG_TCASE(CONV_COPY, 8) PMG_TCASE(CONV_COPY, 4) PMG_TCASE(CONV_COPY, 2)
+  PMG_TCASE(CONV_COPY, 1)
+  PMG_TCASE(CONV_E4M3_BF16, 16) PMG_TCASE(CONV_E4M3_BF16, 4) PMG_TCASE(CONV_E4M3_BF16, 1)
+  PMG_TCASE(CONV_E4M3_F16, 16) PMG_TCASE(CONV_E4M3_F16, 4) PMG_TCASE(CONV_E4M3_F16, 1)
+  PMG_TCASE(CONV_E4M3_F32, 16) PMG_TCASE(CONV_E4M3_F32, 4) PMG_TCASE(CONV_E4M3_F32, 1)
+  PMG_TCASE(CONV_BF16_F32, 8) PMG_TCASE(CONV_BF16_F32, 2) PMG_TCASE(CONV_BF16_F32, 1)
+  PMG_TCASE(CONV_F16_F32, 8) PMG_TCASE(CONV_F16_F32, 2) PMG_TCASE(CONV_F16_F32, 1)
+#undef PMG_TCASE
   return nullptr;
 }
 
@@ -1768,6 +1903,78 @@ int pmg_gather_ex(const void* cache, int64_t cache_block_stride, int64_t cache_t
   if (st != PMG_OK) return st;
   if (pl.path == PMG_PATH_NONE) return PMG_OK;
   return launch_gather(pl, static_cast<cudaStream_t>(stream));
+}
+
+int pmg_gather_tokens(const void* cache, int64_t cache_block_stride, int64_t cache_token_stride, int64_t num_blocks,
+                      const int32_t* block_table, int64_t block_table_stride, const int32_t* token_to_seq,
+                      const int32_t* cu_seq_lens, int32_t num_reqs, int64_t num_tokens, int32_t block_size,
+                      int32_t entry_size, int32_t src_dtype, int32_t dst_dtype, const float* scale, void* dst,
+                      int64_t dst_token_stride, int32_t* error_flag, void* stream, uint32_t options) {
+  const int conv = conv_of(src_dtype, dst_dtype);
+  if (conv < 0) return PMG_ERR_DTYPE;
+  if (num_reqs < 0 || num_tokens < 0 || block_size < 1 || entry_size < 1 || num_blocks < 0 ||
+      block_table_stride < 0 || cache_block_stride < 0 || cache_token_stride < 0 || dst_token_stride < entry_size)
+    return PMG_ERR_ARG;
+  if (options & ~PMG_OPT_FORCE_SCALAR) return PMG_ERR_ARG;
+  const int es = elem_bytes(src_dtype), ed = elem_bytes(dst_dtype);
+  if (static_cast<int64_t>(entry_size) * ed > INT32_MAX || num_tokens > INT32_MAX) return PMG_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return PMG_OK;
+  if (token_to_seq == nullptr || dst == nullptr) return PMG_ERR_NULL;
+  if (num_reqs > 0 && (cache == nullptr || block_table == nullptr || cu_seq_lens == nullptr)) return PMG_ERR_NULL;
+  if (!aligned(cache, es) || !aligned(dst, ed) || !aligned(block_table, 4) || !aligned(token_to_seq, 4) ||
+      !aligned(cu_seq_lens, 4) || (scale != nullptr && !aligned(scale, 4)) ||
+      (error_flag != nullptr && !aligned(error_flag, 4)))
+    return PMG_ERR_ALIGN;
+  if (cache_block_stride > INT64_MAX / es / 2 || cache_token_stride > INT64_MAX / es / 2 ||
+      dst_token_stride > INT64_MAX / ed / 2)
+    return PMG_ERR_ARG;
+  TokParams q{};
+  q.cache = static_cast<const uint8_t*>(cache);
+  q.blk_stride_b = cache_block_stride * es;
+  q.tok_stride_b = cache_token_stride * es;
+  q.num_blocks = num_blocks;
+  q.bt = block_table;
+  q.bt_stride = block_table_stride;
+  q.t2s = token_to_seq;
+  q.cu = cu_seq_lens;
+  q.T = num_tokens;
+  q.R = num_reqs;
+  q.B = block_size;
+  q.dst = static_cast<uint8_t*>(dst);
+  q.dst_stride_b = dst_token_stride * ed;
+  q.scale = scale;
+  q.err = error_flag;
+  int unit = pick_unit(conv, es, ed, entry_size, cache, q.blk_stride_b, q.tok_stride_b, dst, q.dst_stride_b);
+  if (options & PMG_OPT_FORCE_SCALAR) unit = (conv == CONV_COPY) ? es : 1;
+  const int64_t upr = (conv == CONV_COPY) ? static_cast<int64_t>(entry_size) * es / unit : entry_size / unit;
+  if (32ull * static_cast<uint64_t>(upr) >= (1ull << 32)) return PMG_ERR_UNSUPPORTED;
+  q.units_per_row = static_cast<int32_t>(upr);
+  uint32_t l = 0;
+  while ((1ull << l) < static_cast<uint64_t>(upr)) ++l;
+  q.upr_magic = static_cast<uint32_t>((((1ull << l) - static_cast<uint64_t>(upr)) << 32) / static_cast<uint64_t>(upr) + 1);
+  q.upr_shift = static_cast<int32_t>(l);
+  TokKernelFn k = tokens_kernel_for(conv, unit);
+  if (k == nullptr) return PMG_ERR_UNSUPPORTED;
+  int sms = 0;
+  int st = device_setup(&sms);
+  if (st != PMG_OK) return st;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kTokThreads, 0) != cudaSuccess || per_sm < 1)
+    return PMG_ERR_CUDA;
+  const int64_t tiles = (num_tokens + 31) / 32;
+  const int64_t need = (tiles + kTokThreads / 32 - 1) / (kTokThreads / 32);
+  const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(static_cast<int64_t>(per_sm) * sms, need));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kTokThreads);
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = use_pdl() ? 1 : 0;
+  if (cudaLaunchKernelEx(&cfg, k, q) != cudaSuccess) return PMG_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? PMG_OK : PMG_ERR_CUDA;
 }
 
 int pmg_gather(const void* cache, int64_t cache_block_stride, int64_t cache_token_stride, int64_t num_blocks,
