@@ -188,13 +188,28 @@ def run_ours(args, wl: W.Workload, ws: int, rank: int, local: int):
     # one scheduling workspace serves every call on this stream
     ws_buf = None if args.no_workspace else binding.new_workspace(dev)
 
+    if args.entry == "tokens":
+        # the per-token entry point: each output row names its request
+        cu_h = wl.cu_seq_lens.numpy()
+        t2s_h = np.full(wl.total_tokens, -1, np.int32)
+        for r in range(wl.num_reqs):
+            t2s_h[cu_h[r]:min(cu_h[r + 1], wl.total_tokens)] = r
+        for r in reps:
+            r.t2s = torch.from_numpy(t2s_h).to(dev)
+
     def step(k, strm=None):
         r = reps[k % nrep]
-        binding.gather(r.cache, r.dst, r.bt, r.cu, r.ss, r.scale, r.err, num_reqs=wl.num_reqs,
-                       stream=stream if strm is None else strm, options=args.options, workspace=ws_buf)
+        if args.entry == "tokens":
+            binding.gather_tokens(r.cache, r.dst, r.bt, r.t2s, r.cu, r.scale, r.err, num_reqs=wl.num_reqs,
+                                  stream=stream if strm is None else strm, options=args.options)
+        else:
+            binding.gather(r.cache, r.dst, r.bt, r.cu, r.ss, r.scale, r.err, num_reqs=wl.num_reqs,
+                           stream=stream if strm is None else strm, options=args.options, workspace=ws_buf)
 
     path, unit = binding.select_path(base.cache, base.dst, base.bt, base.cu, num_reqs=wl.num_reqs,
                                      options=args.options)
+    if args.entry == "tokens":
+        path = "per-token SIMT"
     for k in range(args.warmup):
         step(k)
     torch.cuda.synchronize(dev)
@@ -452,6 +467,8 @@ def main():
     ap.add_argument("--config", default="60k", choices=sorted(W.CONFIGS))
     ap.add_argument("--quick", action="store_true", help="skip the cold, e2e and CPU-baseline legs")
     ap.add_argument("--options", type=int, default=0, help="PMG_OPT_* bits passed to every call (path sweeps)")
+    ap.add_argument("--entry", choices=["gather", "tokens"], default="gather",
+                    help="gather: the page gather (default); tokens: the per-token indexed gather")
     ap.add_argument("--no-workspace", action="store_true",
                     help="static work split (no scheduling workspace) for comparison")
     args = ap.parse_args()

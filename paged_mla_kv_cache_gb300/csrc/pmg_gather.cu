@@ -1173,7 +1173,8 @@ __global__ void __launch_bounds__(kCvtThreads) gather_tma_convert_kernel(const _
 // t - cu_seq_lens[b]. One warp takes 32 consecutive tokens: each lane resolves
 // its token (request id, row range, block-table column, block id, all masked),
 // then the warp moves the 32 rows as a flat run of vector units, each lane
-// fetching the row base of its unit from the owning lane by shuffle.
+// fetching the row base of its unit from the owning lane by shuffle. Small
+// calls use tiles of 16 or 8 tokens so that every resident warp has work.
 // ---------------------------------------------------------------------------
 
 struct TokParams {
@@ -1195,6 +1196,7 @@ struct TokParams {
   int32_t units_per_row;
   uint32_t upr_magic;
   int32_t upr_shift;
+  int32_t tile_rows;  // tokens per warp tile: 8, 16 or 32
 };
 
 constexpr int kTokThreads = 256;
@@ -1213,11 +1215,12 @@ __global__ void __launch_bounds__(kTokThreads) gather_tokens_kernel(const __grid
   const uint64_t keep = evict_last_policy();
   const uint32_t upr = static_cast<uint32_t>(p.units_per_row);
   int bits = 0;
-  for (int64_t tile = static_cast<int64_t>(blockIdx.x) * (kTokThreads / 32) + (threadIdx.x >> 5); tile * 32 < p.T;
+  const int64_t tr = p.tile_rows;
+  for (int64_t tile = static_cast<int64_t>(blockIdx.x) * (kTokThreads / 32) + (threadIdx.x >> 5); tile * tr < p.T;
        tile += warps) {
-    const int64_t t = tile * 32 + lane;
+    const int64_t t = tile * tr + lane;
     int64_t src = -1;
-    if (t < p.T) {
+    if (lane < tr && t < p.T) {
       const int32_t b = __ldg(p.t2s + t);
       if (b < 0 || b >= p.R) {
         bits |= PMG_FLAG_TOKEN;
@@ -1244,8 +1247,8 @@ __global__ void __launch_bounds__(kTokThreads) gather_tokens_kernel(const __grid
       }
     }
     const int64_t dst_row = t * p.dst_stride_b;
-    const int64_t left = p.T - tile * 32;
-    const uint32_t nrows = static_cast<uint32_t>(left < 32 ? left : 32);
+    const int64_t left = p.T - tile * tr;
+    const uint32_t nrows = static_cast<uint32_t>(left < tr ? left : tr);
     const uint32_t total = nrows * upr;
     for (uint32_t base = 0; base < total; base += 32u * kUnroll) {
       Raw<kInBytes> in[kUnroll];
@@ -1961,7 +1964,15 @@ int pmg_gather_tokens(const void* cache, int64_t cache_block_stride, int64_t cac
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kTokThreads, 0) != cudaSuccess || per_sm < 1)
     return PMG_ERR_CUDA;
-  const int64_t tiles = (num_tokens + 31) / 32;
+  // smaller tiles until there are at least four per resident warp
+  const int64_t resident_warps = static_cast<int64_t>(per_sm) * sms * (kTokThreads / 32);
+  int32_t tr = 32;
+  while (tr > 8 && (num_tokens + tr - 1) / tr < 4 * resident_warps) tr /= 2;
+  // PMG_TOKEN_TILE (8, 16 or 32) overrides the choice for tuning sweeps
+  static const int tile_env = env_int("PMG_TOKEN_TILE", 0, 0, 32);
+  if (tile_env == 8 || tile_env == 16 || tile_env == 32) tr = tile_env;
+  q.tile_rows = tr;
+  const int64_t tiles = (num_tokens + tr - 1) / tr;
   const int64_t need = (tiles + kTokThreads / 32 - 1) / (kTokThreads / 32);
   const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(static_cast<int64_t>(per_sm) * sms, need));
   cudaLaunchConfig_t cfg = {};

@@ -132,3 +132,14 @@ def test_single_300k_tokens():
     wl = W.single_300k()
     t2s, cu = _consistent(wl)
     _run(wl, t2s, cu)
+
+
+@pytest.mark.parametrize("T", [500_000, 1_000_000])
+def test_many_small_rows_use_the_larger_tiles(T):
+    """Enough tokens for 16- and 32-token warp tiles (small calls use 8)."""
+    rng = np.random.default_rng(T % 97)
+    lens = [int(x) for x in rng.integers(1, 2 * T // 50, 50)]
+    lens[-1] += T - sum(lens) if T > sum(lens) else 0
+    wl = W.make_workload("tok", lens, None, 64, 8, None, "fp8_e4m3", "bf16", 0.05, 38)
+    t2s, cu = _consistent(wl)
+    _run(wl, t2s, cu)
