@@ -379,3 +379,49 @@ def test_int64_output_offsets_fp32_1m_tokens():
                     torch.tensor([0, T], dtype=torch.int32), torch.tensor([17], dtype=torch.int32), [T], 1, T, B, E,
                     "fp32", "fp32", 1.0)
     _check(wl)
+
+
+# --- the context-parallel calling pattern: a slice of a larger workspace ------
+
+@pytest.mark.parametrize("name", ["skew8", "skew64_raw"])
+def test_cp_workspace_slice_eager_and_graph(name):
+    """The page's context-parallel prefill gathers into workspace[:toks] and
+    leaves the workspace tail to an all-gather (section "实现拆解" item 2). Here
+    the gather writes rows [off, off + T) of a larger workspace, from an eager
+    call and from a captured CUDA graph; every other row keeps its contents."""
+    wl = W.CONFIGS[name]()
+    want, oflag = oracle_run(wl)
+    assert oflag == 0
+    dev = "cuda:0"
+    ed = W.ELEM_BYTES[wl.dst_dtype]
+    off, tail = 300, 1000
+    rows = off + wl.total_tokens + tail
+    ws = torch.full((rows, wl.entry_size * ed), 0x3C, dtype=torch.uint8, device=dev)
+    dst = ws.view(W.TORCH_DTYPES[wl.dst_dtype])[off:off + wl.total_tokens]
+    cache = wl.cache.to(dev)[:, :, :wl.entry_size]
+    bt, cu = wl.block_table.to(dev), wl.cu_seq_lens.to(dev)
+    ss = None if wl.seq_starts is None else wl.seq_starts.to(dev)
+    scale = torch.tensor([wl.scale], dtype=torch.float32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    sched = binding.new_workspace(dev)
+
+    def call(stream=None):
+        binding.gather(cache, dst, bt, cu, ss, scale, err, stream=stream, workspace=sched)
+
+    def check():
+        torch.cuda.synchronize()
+        host = ws.cpu().numpy()
+        assert np.all(host[:off] == 0x3C) and np.all(host[off + wl.total_tokens:] == 0x3C)
+        got = host[off:off + wl.total_tokens].view(W.NP_BITS[ed])
+        assert int(err.item()) == 0
+        assert_same(got, want, wl.dst_dtype, wl.src_dtype != wl.dst_dtype)
+
+    call()
+    check()
+    ws.fill_(0x3C)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call(torch.cuda.current_stream())
+    g.replay()
+    g.replay()
+    check()
