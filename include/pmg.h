@@ -79,6 +79,13 @@ typedef enum pmg_status {
 #define PMG_OPT_FORCE_SIMT 1u      /* use the SIMT vector kernel even where TMA bulk applies */
 #define PMG_OPT_FORCE_SCALAR 2u    /* use one-element units (the scalar-stride path) */
 #define PMG_OPT_IMPLIED_END 4u     /* cu_seq_lens has num_reqs entries; the last request ends at total_tokens */
+/* The caller promises that no kernel still running in the stream when this
+ * call starts writes cu_seq_lens, seq_starts, block_table or error_flag. The
+ * TMA paths then read them (plan and first block ids) while the previous grid
+ * finishes, under programmatic dependent launch; the cache, the scale, the
+ * workspace and dst are still touched only after the previous grid completes.
+ * Ignored by the SIMT paths and for more than PMG_MAX_REQS_PLAN requests. */
+#define PMG_OPT_EARLY_METADATA 8u
 
 /* Data-movement paths (pmg_select_path). */
 typedef enum pmg_path {

@@ -38,6 +38,7 @@ FLAG_TOKEN = 32
 OPT_FORCE_SIMT = 1
 OPT_FORCE_SCALAR = 2
 OPT_IMPLIED_END = 4
+OPT_EARLY_METADATA = 8
 
 PATH_NAMES = {0: "none", 1: "bulk", 2: "vector", 3: "scalar"}
 WORKSPACE_INTS = 4

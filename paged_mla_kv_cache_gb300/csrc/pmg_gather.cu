@@ -89,6 +89,7 @@ struct Params {
   int32_t* err;           // may be null
   int32_t* sched;         // work-claim counter in the caller's workspace, or null (static split)
   const int32_t* gate;    // large batches: non-zero when cu_seq_lens failed validation (write nothing)
+  int32_t early;          // plan and first block ids before the previous grid completes (caller's promise)
   int32_t sched_static_pct;  // dynamic mode: share of rows split statically up front
   int32_t sched_min_rows;    // dynamic mode only when rows per CTA reach this
   // SIMT mover
@@ -136,9 +137,11 @@ __device__ __forceinline__ int32_t ld_meta(const int32_t* ptr, uint64_t pol) {
 // Programmatic dependent launch: let the next kernel in the stream begin its
 // launch now, and wait until the previous kernel's writes are visible before
 // this grid reads any input. Both are no-ops for a normal launch.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_entry() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  pdl_trigger();
+  pdl_wait();
 }
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -615,10 +618,13 @@ __device__ bool run_scheduler(const Params& p, const PlanView& v, int32_t num_ta
     its = make_items(v, p);
     have = k < its.n;
   }
+  // with early metadata the workspace (claim counter) is touched only after
+  // the previous grid is done: wait after the first published batch
+  bool waited = p.early == 0;
   while (have) {
     // claim the next item now; its latency overlaps this item's resolution
     uint32_t claimed = 0;
-    if (its.dynamic && lane == 0) claimed = gridDim.x + atomicAdd(reinterpret_cast<unsigned*>(p.sched), 1u);
+    if (its.dynamic && lane == 0 && waited) claimed = gridDim.x + atomicAdd(reinterpret_cast<unsigned*>(p.sched), 1u);
     uint32_t r0, r1;
     item_rows(its, k, r0, r1);
     if (r0 < r1) {
@@ -640,6 +646,11 @@ __device__ bool run_scheduler(const Params& p, const PlanView& v, int32_t num_ta
         t += kSegCap;
       }
     }
+    if (!waited) {
+      pdl_wait();
+      waited = true;
+      if (its.dynamic && lane == 0) claimed = gridDim.x + atomicAdd(reinterpret_cast<unsigned*>(p.sched), 1u);
+    }
     if (its.dynamic) {
       k = __shfl_sync(0xffffffffu, claimed, 0);
       have = k < its.n;
@@ -652,6 +663,7 @@ __device__ bool run_scheduler(const Params& p, const PlanView& v, int32_t num_ta
       have = false;
     }
   }
+  if (!waited) pdl_wait();
   const int b = static_cast<int>(uses % kSegBufs);
   if (uses >= kSegBufs && !mbar_wait_bounded(&q.empty[b], ((uses / kSegBufs) - 1u) & 1u)) return false;
   if (lane == 0) q.count[b] = -1;
@@ -732,7 +744,12 @@ __global__ void __launch_bounds__(kBulkThreads) gather_bulk_kernel(const __grid_
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   prefetch_metadata(p);
-  pdl_entry();
+  pdl_trigger();
+  // With early metadata the scheduler warp plans and resolves its first batch
+  // while the previous grid may still run; every read of the cache, scale or
+  // workspace and every write of dst comes after the wait.
+  const bool early = p.early != 0;
+  if (!early) pdl_wait();
   if (p.gate != nullptr && *reinterpret_cast<const volatile int32_t*>(p.gate) != 0) return;
   __syncthreads();
   // small batches: the scheduler warp plans alone; large ones: the whole CTA
@@ -747,6 +764,7 @@ __global__ void __launch_bounds__(kBulkThreads) gather_bulk_kernel(const __grid_
     if (warp_plan) num_tasks = build_plan<true>(p, v, blockIdx.x == 0);
     if (!run_scheduler(p, v, num_tasks, q)) set_flag(p, PMG_FLAG_TIMEOUT);
   } else if (tid == 0) {
+    if (early) pdl_wait();
     const uint64_t pol = evict_first_policy();
     const uint32_t row_bytes = static_cast<uint32_t>(p.row_src_bytes);
     const uint32_t S = static_cast<uint32_t>(p.stages);
@@ -1086,7 +1104,12 @@ __global__ void __launch_bounds__(kCvtThreads) gather_tma_convert_kernel(const _
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   prefetch_metadata(p);
-  pdl_entry();
+  pdl_trigger();
+  // With early metadata the scheduler warp plans and resolves its first batch
+  // while the previous grid may still run; every read of the cache, scale or
+  // workspace and every write of dst comes after the wait.
+  const bool early = p.early != 0;
+  if (!early) pdl_wait();
   if (p.gate != nullptr && *reinterpret_cast<const volatile int32_t*>(p.gate) != 0) return;
   __syncthreads();
   // small batches: the scheduler warp plans alone; large ones: the whole CTA
@@ -1103,6 +1126,7 @@ __global__ void __launch_bounds__(kCvtThreads) gather_tma_convert_kernel(const _
   } else if (warp == kCvtWarps) {
     // producer: one lane issues the bulk loads, up to p.stages chunks ahead
     if (lane == 0) {
+      if (early) pdl_wait();
       const uint64_t pol = evict_first_policy();
       const uint32_t S = static_cast<uint32_t>(p.stages);
       SegReader rd{0, -1, 0, ChunkIter{0, 0}, false};
@@ -1128,6 +1152,7 @@ __global__ void __launch_bounds__(kCvtThreads) gather_tma_convert_kernel(const _
     }
   } else {
     // converters: every landed stage, unit u = (row, col) of the chunk
+    if (early) pdl_wait();
     float scale = 1.0f;
     if (CONV == CONV_E4M3_BF16 || CONV == CONV_E4M3_F16 || CONV == CONV_E4M3_F32) {
       if (p.scale != nullptr) scale = __ldg(p.scale);
@@ -1482,7 +1507,8 @@ int make_plan(const void* cache, int64_t cbs, int64_t cts, int64_t num_blocks, c
   if (conv < 0) return PMG_ERR_DTYPE;
   if (R < 0 || T < 0 || B < 1 || E < 1 || num_blocks < 0 || bt_stride < 0 || cbs < 0 || cts < 0 || dts < E)
     return PMG_ERR_ARG;
-  if (options & ~(PMG_OPT_FORCE_SIMT | PMG_OPT_FORCE_SCALAR | PMG_OPT_IMPLIED_END)) return PMG_ERR_ARG;
+  if (options & ~(PMG_OPT_FORCE_SIMT | PMG_OPT_FORCE_SCALAR | PMG_OPT_IMPLIED_END | PMG_OPT_EARLY_METADATA))
+    return PMG_ERR_ARG;
   if (R > PMG_MAX_REQS) return PMG_ERR_UNSUPPORTED;
   // more requests than one launch plans need the workspace (for the verdict
   // of the whole-array validation)
@@ -1522,6 +1548,8 @@ int make_plan(const void* cache, int64_t cbs, int64_t cts, int64_t num_blocks, c
   q.scale = scale;
   q.err = err;
   q.sched = workspace;
+  // large batches read a verdict from the workspace first: no early start there
+  q.early = ((options & PMG_OPT_EARLY_METADATA) && R <= PMG_MAX_REQS_PLAN) ? 1 : 0;
   q.sched_static_pct = sched_static_pct();
   q.sched_min_rows = sched_min_rows();
   out.conv = conv;

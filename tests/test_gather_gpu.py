@@ -81,6 +81,33 @@ def test_workspace_reuse_across_calls_and_graph_replays(name):
     assert_same(got, want, wl.dst_dtype, wl.src_dtype != wl.dst_dtype)
 
 
+@pytest.mark.parametrize("name", ["tiny", "60k", "300k", "skew8", "skew64_raw", "skew64_dequant"])
+@pytest.mark.parametrize("workspace", [False, True])
+def test_named_workloads_early_metadata(name, workspace):
+    """PMG_OPT_EARLY_METADATA: the plan runs before the previous grid is done;
+    the result is the same."""
+    _check(W.CONFIGS[name](), options=binding.OPT_EARLY_METADATA, workspace=workspace)
+
+
+@pytest.mark.parametrize("name", ["60k", "skew8", "skew64_dequant"])
+def test_early_metadata_back_to_back_graph(name):
+    """Back-to-back calls replayed from a CUDA graph with early metadata: each
+    call overlaps the previous one's tail; outputs and the workspace stay right."""
+    wl = W.CONFIGS[name]()
+    want, _ = oracle_run(wl)
+    case = DeviceCase(wl, workspace=True)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        s = torch.cuda.current_stream()
+        for _ in range(4):
+            case.run(options=binding.OPT_EARLY_METADATA, stream=s)
+    for _ in range(3):
+        g.replay()
+    got, flag, guards = case.result()
+    assert guards and flag == 0
+    assert_same(got, want, wl.dst_dtype, wl.src_dtype != wl.dst_dtype)
+
+
 @pytest.mark.parametrize("name", ["tiny", "60k", "skew8", "skew64_raw"])
 @pytest.mark.parametrize("options", [binding.OPT_FORCE_SIMT, binding.OPT_FORCE_SCALAR])
 def test_named_workloads_other_paths(name, options):
