@@ -86,9 +86,18 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def kernel_code_hash(text: str) -> str:
+    """sha256 of the kernel source with comments and blank lines removed, so a
+    comment edit does not count as a kernel change."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    lines = [line.rstrip() for line in text.splitlines() if line.strip()]
+    return hashlib.sha256("\n".join(lines).encode()).hexdigest()
+
+
 def profiled_traffic(config: str):
     """DRAM bytes per launch from the committed ncu summary of this workload, if
-    it was taken on the current kernel source (else None)."""
+    it was taken on the current kernel code (else None)."""
     name = PROFILE_FILES.get(config)
     if name is None:
         return None
@@ -96,11 +105,11 @@ def profiled_traffic(config: str):
         text = open(os.path.join(ROOT, "profiles", name)).read()
     except OSError:
         return None
-    m_sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    m_sha = re.search(r"kernel_code_sha256:\s*([0-9a-f]{64})", text)
     m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
     if not (m_sha and m_tr):
         return None
-    sha = hashlib.sha256(open(KERNEL_SRC, "rb").read()).hexdigest()
+    sha = kernel_code_hash(open(KERNEL_SRC).read())
     return int(m_tr.group(1)) if sha == m_sha.group(1) else None
 
 

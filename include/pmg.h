@@ -90,7 +90,8 @@ typedef enum pmg_status {
 /* Data-movement paths (pmg_select_path). */
 typedef enum pmg_path {
   PMG_PATH_NONE = 0,   /* nothing to do (no rows or no requests): no launch */
-  PMG_PATH_BULK = 1,   /* TMA 1-D bulk copies global -> shared -> global (byte copy, 16-B aligned rows) */
+  PMG_PATH_BULK = 1,   /* TMA 1-D bulk loads of 16-B aligned source rows into a shared ring; byte copies
+                          leave by bulk stores, converting gathers by 16-byte stores of converter warps */
   PMG_PATH_VECTOR = 2, /* SIMT loads/stores of several elements per thread */
   PMG_PATH_SCALAR = 3  /* SIMT, one element per access (any alignment) */
 } pmg_path;

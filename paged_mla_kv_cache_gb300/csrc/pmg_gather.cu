@@ -13,22 +13,30 @@
 //
 // How this file does it (GB300-first, not the page's kernel):
 //  * Work split. The page gives one CTA per logical page. Here a persistent
-//    grid (a multiple of the SM count) splits the OUTPUT ROWS evenly across
-//    CTAs, so a 300K-token request and a 17-token request cost each CTA the
-//    same bytes; inside its row range a CTA walks page tasks in order.
-//  * Page-task mapper. Every CTA builds, in shared memory, the exclusive prefix
-//    sum of per-request page counts (a block scan over requests). A flat task
-//    id becomes (req, logical_block, page_token_begin, page_token_end,
-//    output_token_begin) by a binary search over that prefix: O(log R) where
-//    the page's mapper scans all requests linearly.
-//  * Broadcast. The tasks of a CTA's range are resolved in parallel (one
-//    thread per task: map, one block-table read, bounds checks) into a
-//    shared-memory segment table that the whole CTA then reads.
-//  * Movement. Byte copies of 16-byte aligned rows use TMA 1-D bulk copies
+//    grid (a multiple of the SM count) splits the OUTPUT ROWS across CTAs, so a
+//    300K-token request and a 17-token request cost each CTA the same bytes;
+//    inside its rows a CTA walks page tasks in order. With a caller workspace,
+//    a quarter of the rows is split up front and the rest is claimed in
+//    stage-sized items through an atomic counter, which evens out CTAs whose
+//    memory traffic is served at different speeds.
+//  * Page-task mapper. The exclusive prefix sum of per-request page counts is
+//    built in shared memory (by one warp for up to 256 requests, by the CTA
+//    up to 4096; larger batches run as groups). A flat task id becomes (req,
+//    logical_block, page_token_begin, page_token_end, output_token_begin) by a
+//    binary search over that prefix: O(log R) where the page's mapper scans
+//    all requests linearly.
+//  * Broadcast. A scheduler warp resolves the tasks of the next work item one
+//    per lane (map, one block-table read, bounds checks) into a shared-memory
+//    segment queue while the current item's copies are in flight.
+//  * Movement. Byte copies of 16-byte aligned rows use a TMA 1-D bulk ring
 //    (cp.async.bulk global -> shared with an mbarrier, then shared -> global
-//    bulk stores), a multi-stage ring per CTA driven by one thread. Converts and
-//    unaligned layouts use SIMT loads and stores of 16, 8, 4, 2 or 1 bytes per
-//    access with the convert done in registers.
+//    bulk stores) driven by one thread. Converting gathers bulk-load source
+//    rows into a ring that converter warps turn into 16-byte stores. Rows that
+//    are not 16-byte aligned take SIMT loads and stores of 16, 8, 4, 2 or 1
+//    bytes. A per-token variant maps each output row through token_to_seq.
+//  * Launch. Programmatic dependent launch: metadata is prefetched into L2
+//    while the previous grid finishes; inputs are read only after it completes
+//    (or, with the caller's early-metadata promise, the plan runs before).
 //  * Safety. 64-bit byte offsets everywhere; the logical block is checked
 //    against block_table_stride and the physical id against num_blocks in
 //    every path (the review section "评论区精华" reports both checks missing
