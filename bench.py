@@ -160,6 +160,13 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def workload_config(wl: W.Workload) -> dict:
+    """The keys that name the workload, shared by both arms."""
+    return {"workload": wl.name, "num_reqs": wl.num_reqs, "total_tokens": wl.total_tokens,
+            "block_size": wl.block_size, "entry_size": wl.entry_size, "num_blocks": wl.num_blocks,
+            "cache_dtype": wl.src_dtype, "out_dtype": wl.dst_dtype, "bytes_per_step": wl.algorithmic_bytes()}
+
+
 def make_workload(name: str) -> W.Workload:
     return W.CONFIGS[name]()
 
@@ -337,18 +344,10 @@ def run_ours(args, wl: W.Workload, ws: int, rank: int, local: int):
         "dtype": "bf16" if wl.src_dtype == wl.dst_dtype == "bf16" else f"{wl.src_dtype}->{wl.dst_dtype}",
         "data": "synthetic (seeded N(0,1) cache, seeded block-id permutation)",
         "config": {
-            "workload": wl.name,
-            "num_reqs": wl.num_reqs,
-            "total_tokens": wl.total_tokens,
-            "block_size": wl.block_size,
-            "entry_size": wl.entry_size,
-            "num_blocks": wl.num_blocks,
-            "cache_dtype": wl.src_dtype,
-            "out_dtype": wl.dst_dtype,
+            **workload_config(wl),
             "path": path if args.options == 0 else f"{path} (options {args.options})",
             "schedule": ("static" if args.no_workspace else "dynamic (workspace)")
                         + (", early metadata" if args.early_metadata else ""),
-            "bytes_per_step": alg_bytes,
             "l2": f"{nrep} rotating input replicas ({sum(r.nbytes() for r in reps) / 1e6:.0f} MB) > 4x L2; no flush",
             "parallelism": f"replicas x{ws}",
         },
@@ -488,8 +487,7 @@ def run_reference(args, wl, ws, rank):
         "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": wl.src_dtype, "data": "synthetic",
-        "config": {"workload": wl.name, "num_reqs": wl.num_reqs, "total_tokens": wl.total_tokens,
-                   "block_size": wl.block_size, "entry_size": wl.entry_size},
+        "config": {**workload_config(wl), "path": "CPU oracle (per-token loop)"},
         "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
