@@ -218,7 +218,7 @@ def run_ours(args, wl: W.Workload, ws: int, rank: int, local: int):
         opts = args.options if options is None else options
         if args.entry == "tokens":
             binding.gather_tokens(r.cache, r.dst, r.bt, r.t2s, r.cu, r.scale, r.err, num_reqs=wl.num_reqs,
-                                  stream=stream if strm is None else strm, options=opts)
+                                  stream=stream if strm is None else strm, options=opts, workspace=ws_buf)
         else:
             binding.gather(r.cache, r.dst, r.bt, r.cu, r.ss, r.scale, r.err, num_reqs=wl.num_reqs,
                            stream=stream if strm is None else strm, options=opts, workspace=ws_buf)
@@ -226,7 +226,7 @@ def run_ours(args, wl: W.Workload, ws: int, rank: int, local: int):
     path, unit = binding.select_path(base.cache, base.dst, base.bt, base.cu, num_reqs=wl.num_reqs,
                                      options=args.options)
     if args.entry == "tokens":
-        path = "per-token SIMT"
+        path = "per-token " + ("SIMT" if path != "bulk" else "bulk")
     for k in range(args.warmup):
         step(k)
     torch.cuda.synchronize(dev)

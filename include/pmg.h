@@ -216,7 +216,15 @@ int pmg_gather_noalloc(const void* cache, int64_t cache_block_stride, int64_t ca
  *  cu_seq_lens    int32 [num_reqs + 1], device: request b owns output rows
  *                 [cu[b], cu[b+1]); row t reads context position t - cu[b].
  *  num_tokens     rows of dst to produce, 0 <= num_tokens <= INT32_MAX.
- *  options        0 or PMG_OPT_FORCE_SCALAR.
+ *  workspace      NULL, or PMG_WORKSPACE_INTS zeroed int32 on the device
+ *                 (16-byte aligned), as in pmg_gather_ex: it lets the TMA
+ *                 path balance rows across CTAs dynamically.
+ *  options        bitwise OR of PMG_OPT_FORCE_SIMT, PMG_OPT_FORCE_SCALAR and
+ *                 PMG_OPT_EARLY_METADATA (read for token_to_seq as well).
+ *                 Without a FORCE option, rows whose 16-byte alignment fits
+ *                 the TMA path (PMG_PATH_BULK of pmg_select_path) go through
+ *                 it: consecutive tokens whose cache rows are adjacent travel
+ *                 as one bulk copy. Otherwise a SIMT kernel copies each row.
  * Every other argument is as in pmg_gather (there is no seq_starts). Output
  * row t = convert(cache[block_table[b, p / block_size], p % block_size]) with
  * b = token_to_seq[t], p = t - cu[b]. Every index is checked before use: a
@@ -229,7 +237,8 @@ int pmg_gather_tokens(const void* cache, int64_t cache_block_stride, int64_t cac
                       const int32_t* block_table, int64_t block_table_stride, const int32_t* token_to_seq,
                       const int32_t* cu_seq_lens, int32_t num_reqs, int64_t num_tokens, int32_t block_size,
                       int32_t entry_size, int32_t src_dtype, int32_t dst_dtype, const float* scale, void* dst,
-                      int64_t dst_token_stride, int32_t* error_flag, void* stream, uint32_t options);
+                      int64_t dst_token_stride, int32_t* error_flag, int32_t* workspace, void* stream,
+                      uint32_t options);
 
 /*
  * pmg_select_path — host-only: validates the layout arguments of a gather the

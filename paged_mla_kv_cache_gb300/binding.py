@@ -80,7 +80,7 @@ def load_library() -> ctypes.CDLL:
         L.pmg_gather_noalloc.argtypes = gather_args
         L.pmg_gather_tokens.restype = ctypes.c_int
         L.pmg_gather_tokens.argtypes = [vp, i64, i64, i64, vp, i64, vp, vp, i32, i64, i32, i32, i32, i32, vp, vp, i64,
-                                        vp, vp, u32]
+                                        vp, vp, vp, u32]
         L.pmg_select_path.restype = ctypes.c_int
         L.pmg_select_path.argtypes = [vp, i64, i64, i64, vp, i64, vp, i32, i64, i32, i32, i32, i32, vp, i64, u32,
                                       ctypes.POINTER(i32), ctypes.POINTER(i32)]
@@ -185,10 +185,10 @@ def gather_noalloc(cache: torch.Tensor, dst: torch.Tensor, block_table: torch.Te
 def gather_tokens(cache: torch.Tensor, dst: torch.Tensor, block_table: torch.Tensor, token_to_seq: torch.Tensor,
                   cu_seq_lens: torch.Tensor, scale: Optional[torch.Tensor] = None,
                   error_flag: Optional[torch.Tensor] = None, num_reqs: Optional[int] = None, stream=None,
-                  options: int = 0) -> None:
+                  options: int = 0, workspace: Optional[torch.Tensor] = None) -> None:
     """Per-token indexed gather (pmg_gather_tokens): dst row t comes from
     request token_to_seq[t] at position t - cu_seq_lens[token_to_seq[t]].
-    dst has num_tokens = len(token_to_seq) rows used."""
+    dst has num_tokens = len(token_to_seq) rows used. workspace as in gather()."""
     src_code, dst_code = _layout(cache, dst)
     if num_reqs is None:
         num_reqs = cu_seq_lens.shape[0] - 1
@@ -196,7 +196,7 @@ def gather_tokens(cache: torch.Tensor, dst: torch.Tensor, block_table: torch.Ten
         _ptr(cache), cache.stride(0), cache.stride(1), cache.shape[0],
         _ptr(block_table), _table_width(block_table), _ptr(token_to_seq), _ptr(cu_seq_lens), int(num_reqs),
         token_to_seq.shape[0], cache.shape[1], cache.shape[2], src_code, dst_code, _ptr(scale),
-        _ptr(dst), dst.stride(0), _ptr(error_flag), _stream_handle(stream), int(options))
+        _ptr(dst), dst.stride(0), _ptr(error_flag), _ptr(workspace), _stream_handle(stream), int(options))
     if st != PMG_OK:
         raise PmgError(st, "pmg_gather_tokens")
 

@@ -98,6 +98,8 @@ struct Params {
   int32_t* sched;         // work-claim counter in the caller's workspace, or null (static split)
   const int32_t* gate;    // large batches: non-zero when cu_seq_lens failed validation (write nothing)
   int32_t early;          // plan and first block ids before the previous grid completes (caller's promise)
+  const int32_t* t2s;     // per-token gather: request of each output row (token mode)
+  int32_t token_mode;     // 1: rows [0, T) map through t2s instead of the page plan
   int32_t sched_static_pct;  // dynamic mode: share of rows split statically up front
   int32_t sched_min_rows;    // dynamic mode only when rows per CTA reach this
   // SIMT mover
@@ -313,6 +315,17 @@ __device__ __forceinline__ void prefetch_lines(const void* ptr, int64_t bytes, i
 
 __device__ __forceinline__ void prefetch_metadata(const Params& p) {
   const int64_t R = p.R;
+  if (p.token_mode) {
+    // token_to_seq spread over the grid; cu_seq_lens and the block table while small
+    prefetch_lines(p.t2s, static_cast<int64_t>(p.T) * 4, static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x,
+                   static_cast<int64_t>(gridDim.x) * blockDim.x);
+    if ((R + 1) * 4 <= (64ll << 10)) prefetch_lines(p.cu, (R + 1) * 4, threadIdx.x, blockDim.x);
+    const int64_t tb = R * p.bt_stride * 4;
+    if (tb <= (4ll << 20))
+      prefetch_lines(p.bt, tb, static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x,
+                     static_cast<int64_t>(gridDim.x) * blockDim.x);
+    return;
+  }
   const int64_t cu_n = p.implied_end ? R : R + 1;
   prefetch_lines(p.cu, cu_n * 4, threadIdx.x, blockDim.x);
   prefetch_lines(p.ss, R * 4, threadIdx.x, blockDim.x);
@@ -559,8 +572,8 @@ struct Items {
 // are about rows / (16 G) rows and never smaller than one ring stage.
 __device__ __forceinline__ Items make_items(const PlanView& v, const Params& p) {
   Items it;
-  it.lo = static_cast<uint32_t>(v.ob[0]);
-  it.hi = static_cast<uint32_t>(v.ob[p.R]);
+  it.lo = p.token_mode ? 0u : static_cast<uint32_t>(v.ob[0]);
+  it.hi = p.token_mode ? static_cast<uint32_t>(p.T) : static_cast<uint32_t>(v.ob[p.R]);
   const uint32_t rows = it.hi - it.lo;
   const uint32_t G = gridDim.x;
   it.dynamic = p.sched != nullptr && rows / G >= static_cast<uint32_t>(p.sched_min_rows);
@@ -592,6 +605,68 @@ __device__ __forceinline__ void item_rows(const Items& it, uint32_t k, uint32_t&
   } else {
     r0 = it.lo + G * it.a + (k - G) * it.d;
     r1 = r0 + it.d < it.hi ? r0 + it.d : it.hi;
+  }
+}
+
+// Per-token gather: output token t reads request b = t2s[t] at context position
+// t - cu[b]; every index is checked before use. One lane resolves the tokens
+// t_first + 32 j (j < N, those below t_end) with the loads of each step issued
+// together: t2s, then cu, then the block table. src[j] is the source byte
+// offset of the row, or -1 (flag bits in `bits`; tokens at or past t_end set none).
+constexpr int kTokGroup = 4;
+
+template <int N>
+__device__ __forceinline__ void resolve_tokens(const Params& p, uint32_t t_first, uint32_t t_end, int64_t (&src)[N],
+                                               int& bits) {
+  const uint64_t keep = evict_last_policy();
+  int32_t b[N];
+#pragma unroll
+  for (int j = 0; j < N; ++j) {
+    const uint32_t t = t_first + 32u * j;
+    src[j] = -1;
+    b[j] = t < t_end ? ld_meta(p.t2s + t, keep) : -1;
+    if (t < t_end && (b[j] < 0 || b[j] >= p.R)) {
+      bits |= PMG_FLAG_TOKEN;
+      b[j] = -1;
+    }
+  }
+  int32_t c0[N], c1[N];
+#pragma unroll
+  for (int j = 0; j < N; ++j) {
+    c0[j] = b[j] >= 0 ? ld_meta(p.cu + b[j], keep) : 0;
+    c1[j] = b[j] >= 0 ? ld_meta(p.cu + b[j] + 1, keep) : 0;
+  }
+  int32_t phys[N];
+  uint32_t off[N];
+#pragma unroll
+  for (int j = 0; j < N; ++j) {
+    const int64_t t = static_cast<int64_t>(t_first) + 32 * j;
+    phys[j] = -1;
+    off[j] = 0;
+    if (b[j] < 0) continue;
+    if (t < c0[j] || t >= c1[j]) {
+      bits |= PMG_FLAG_TOKEN;
+      b[j] = -1;
+      continue;
+    }
+    const uint32_t pos = static_cast<uint32_t>(t - c0[j]);
+    const uint32_t lb = pos / static_cast<uint32_t>(p.B);
+    off[j] = pos - lb * static_cast<uint32_t>(p.B);
+    if (static_cast<int64_t>(lb) >= p.bt_stride) {
+      bits |= PMG_FLAG_LOGICAL_BLOCK;
+      b[j] = -1;
+      continue;
+    }
+    phys[j] = ld_meta(p.bt + static_cast<int64_t>(b[j]) * p.bt_stride + lb, keep);
+  }
+#pragma unroll
+  for (int j = 0; j < N; ++j) {
+    if (b[j] < 0) continue;
+    if (phys[j] < 0 || phys[j] >= p.num_blocks) {
+      bits |= PMG_FLAG_PHYS_BLOCK;
+      continue;
+    }
+    src[j] = static_cast<int64_t>(phys[j]) * p.blk_stride_b + static_cast<int64_t>(off[j]) * p.tok_stride_b;
   }
 }
 
@@ -635,7 +710,46 @@ __device__ bool run_scheduler(const Params& p, const PlanView& v, int32_t num_ta
     if (its.dynamic && lane == 0 && waited) claimed = gridDim.x + atomicAdd(reinterpret_cast<unsigned*>(p.sched), 1u);
     uint32_t r0, r1;
     item_rows(its, k, r0, r1);
-    if (r0 < r1) {
+    if (r0 < r1 && p.token_mode) {
+      // 32 tokens per batch, one per lane; consecutive lanes whose source rows
+      // are one slot apart form one segment
+      for (uint32_t g0 = r0; g0 < r1; g0 += 32u * kTokGroup) {
+        int64_t srcs[kTokGroup];
+        int bits = 0;
+        resolve_tokens<kTokGroup>(p, g0 + static_cast<uint32_t>(lane), r1, srcs, bits);
+        if (bits != 0) set_flag(p, bits);
+#pragma unroll
+        for (int j = 0; j < kTokGroup; ++j) {
+          const uint32_t t = g0 + 32u * j + static_cast<uint32_t>(lane);
+          const int64_t src = srcs[j];
+          const int64_t prev = __shfl_up_sync(0xffffffffu, src, 1);
+          const bool valid = src >= 0;
+          const bool cont = lane > 0 && valid && prev >= 0 && src == prev + p.tok_stride_b;
+          const bool start = valid && !cont;
+          const uint32_t starts = __ballot_sync(0xffffffffu, start);
+          const uint32_t breaks = __ballot_sync(0xffffffffu, !cont);
+          const int n = __popc(starts);
+          if (n == 0) continue;
+          const int b = static_cast<int>(uses % kSegBufs);
+          if (uses >= kSegBufs && !mbar_wait_bounded(&q.empty[b], ((uses / kSegBufs) - 1u) & 1u)) return false;
+          if (start) {
+            // the segment runs to the next lane that starts one or is empty
+            const uint32_t after = lane == 31 ? 0u : (breaks & (0xffffffffu << (lane + 1)));
+            const int next = after ? __ffs(after) - 1 : 32;
+            Segment seg;
+            seg.src = src;
+            seg.dst = static_cast<int64_t>(t) * p.dst_stride_b;
+            seg.nrows = next - lane;
+            seg.pad = 0;
+            q.seg[b][__popc(starts & ((1u << lane) - 1u))] = seg;
+          }
+          if (lane == 0) q.count[b] = n;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&q.full[b]);
+          ++uses;
+        }
+      }
+    } else if (r0 < r1) {
       int32_t t = first_task_for_row(v, p.R, p.B, r0);
       for (;;) {
         Segment seg;
@@ -760,8 +874,9 @@ __global__ void __launch_bounds__(kBulkThreads) gather_bulk_kernel(const __grid_
   if (!early) pdl_wait();
   if (p.gate != nullptr && *reinterpret_cast<const volatile int32_t*>(p.gate) != 0) return;
   __syncthreads();
-  // small batches: the scheduler warp plans alone; large ones: the whole CTA
-  const bool warp_plan = p.R <= kWarpPlanMaxReqs;
+  // small batches: the scheduler warp plans alone; large ones: the whole CTA;
+  // the per-token gather needs no plan
+  const bool warp_plan = p.R <= kWarpPlanMaxReqs || p.token_mode;
   int32_t num_tasks = 0;
   if (!warp_plan) {
     num_tasks = build_plan<false>(p, v, blockIdx.x == 0);
@@ -769,7 +884,8 @@ __global__ void __launch_bounds__(kBulkThreads) gather_bulk_kernel(const __grid_
   }
 
   if (warp == 1) {
-    if (warp_plan) num_tasks = build_plan<true>(p, v, blockIdx.x == 0);
+    if (p.token_mode) num_tasks = 1;
+    else if (warp_plan) num_tasks = build_plan<true>(p, v, blockIdx.x == 0);
     if (!run_scheduler(p, v, num_tasks, q)) set_flag(p, PMG_FLAG_TIMEOUT);
   } else if (tid == 0) {
     if (early) pdl_wait();
@@ -1120,8 +1236,9 @@ __global__ void __launch_bounds__(kCvtThreads) gather_tma_convert_kernel(const _
   if (!early) pdl_wait();
   if (p.gate != nullptr && *reinterpret_cast<const volatile int32_t*>(p.gate) != 0) return;
   __syncthreads();
-  // small batches: the scheduler warp plans alone; large ones: the whole CTA
-  const bool warp_plan = p.R <= kWarpPlanMaxReqs;
+  // small batches: the scheduler warp plans alone; large ones: the whole CTA;
+  // the per-token gather needs no plan
+  const bool warp_plan = p.R <= kWarpPlanMaxReqs || p.token_mode;
   int32_t num_tasks = 0;
   if (!warp_plan) {
     num_tasks = build_plan<false>(p, v, blockIdx.x == 0);
@@ -1129,7 +1246,8 @@ __global__ void __launch_bounds__(kCvtThreads) gather_tma_convert_kernel(const _
   }
 
   if (warp == kCvtWarps + 1) {
-    if (warp_plan) num_tasks = build_plan<true>(p, v, blockIdx.x == 0);
+    if (p.token_mode) num_tasks = 1;
+    else if (warp_plan) num_tasks = build_plan<true>(p, v, blockIdx.x == 0);
     if (!run_scheduler(p, v, num_tasks, q)) set_flag(p, PMG_FLAG_TIMEOUT);
   } else if (warp == kCvtWarps) {
     // producer: one lane issues the bulk loads, up to p.stages chunks ahead
@@ -1786,7 +1904,7 @@ int launch_one(const Plan& pl, cudaStream_t stream) {
     KernelFn k = copy ? gather_bulk_kernel : tma_convert_kernel_for(pl.conv);
     if (k == nullptr) return PMG_ERR_UNSUPPORTED;
     const int threads = copy ? kBulkThreads : kCvtThreads;
-    const size_t smem = static_cast<size_t>(q.stages) * q.stage_bytes + host_plan_bytes(q.R);
+    const size_t smem = static_cast<size_t>(q.stages) * q.stage_bytes + (q.token_mode ? 0 : host_plan_bytes(q.R));
     int per_sm = 0;
     if (ctas_per_sm(k, threads, smem, &per_sm) != PMG_OK) return PMG_ERR_CUDA;
     if (per_sm < 1) return PMG_ERR_UNSUPPORTED;
@@ -1948,13 +2066,14 @@ int pmg_gather_tokens(const void* cache, int64_t cache_block_stride, int64_t cac
                       const int32_t* block_table, int64_t block_table_stride, const int32_t* token_to_seq,
                       const int32_t* cu_seq_lens, int32_t num_reqs, int64_t num_tokens, int32_t block_size,
                       int32_t entry_size, int32_t src_dtype, int32_t dst_dtype, const float* scale, void* dst,
-                      int64_t dst_token_stride, int32_t* error_flag, void* stream, uint32_t options) {
+                      int64_t dst_token_stride, int32_t* error_flag, int32_t* workspace, void* stream,
+                      uint32_t options) {
   const int conv = conv_of(src_dtype, dst_dtype);
   if (conv < 0) return PMG_ERR_DTYPE;
   if (num_reqs < 0 || num_tokens < 0 || block_size < 1 || entry_size < 1 || num_blocks < 0 ||
       block_table_stride < 0 || cache_block_stride < 0 || cache_token_stride < 0 || dst_token_stride < entry_size)
     return PMG_ERR_ARG;
-  if (options & ~PMG_OPT_FORCE_SCALAR) return PMG_ERR_ARG;
+  if (options & ~(PMG_OPT_FORCE_SIMT | PMG_OPT_FORCE_SCALAR | PMG_OPT_EARLY_METADATA)) return PMG_ERR_ARG;
   const int es = elem_bytes(src_dtype), ed = elem_bytes(dst_dtype);
   if (static_cast<int64_t>(entry_size) * ed > INT32_MAX || num_tokens > INT32_MAX) return PMG_ERR_UNSUPPORTED;
   if (num_tokens == 0) return PMG_OK;
@@ -1962,11 +2081,28 @@ int pmg_gather_tokens(const void* cache, int64_t cache_block_stride, int64_t cac
   if (num_reqs > 0 && (cache == nullptr || block_table == nullptr || cu_seq_lens == nullptr)) return PMG_ERR_NULL;
   if (!aligned(cache, es) || !aligned(dst, ed) || !aligned(block_table, 4) || !aligned(token_to_seq, 4) ||
       !aligned(cu_seq_lens, 4) || (scale != nullptr && !aligned(scale, 4)) ||
-      (error_flag != nullptr && !aligned(error_flag, 4)))
+      (error_flag != nullptr && !aligned(error_flag, 4)) || (workspace != nullptr && !aligned(workspace, 16)))
     return PMG_ERR_ALIGN;
   if (cache_block_stride > INT64_MAX / es / 2 || cache_token_stride > INT64_MAX / es / 2 ||
       dst_token_stride > INT64_MAX / ed / 2)
     return PMG_ERR_ARG;
+  if (num_reqs > 0 && (options & (PMG_OPT_FORCE_SIMT | PMG_OPT_FORCE_SCALAR)) == 0) {
+    // The TMA pipelines in token mode: the scheduler warp resolves 32 tokens
+    // per batch and merges runs whose source rows are adjacent into segments.
+    // The page plan's checks and path choice run with a single stand-in
+    // request, since token mode plans nothing per request.
+    Plan pl;
+    const int st = make_plan(cache, cache_block_stride, cache_token_stride, num_blocks, block_table,
+                             block_table_stride, cu_seq_lens, nullptr, 1, num_tokens, block_size, entry_size,
+                             src_dtype, dst_dtype, scale, dst, dst_token_stride, error_flag, workspace,
+                             options & PMG_OPT_EARLY_METADATA, pl);
+    if (st == PMG_OK && pl.path == PMG_PATH_BULK) {
+      pl.prm.R = num_reqs;
+      pl.prm.t2s = token_to_seq;
+      pl.prm.token_mode = 1;
+      return launch_one(pl, static_cast<cudaStream_t>(stream));
+    }
+  }
   TokParams q{};
   q.cache = static_cast<const uint8_t*>(cache);
   q.blk_stride_b = cache_block_stride * es;

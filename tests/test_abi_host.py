@@ -136,17 +136,19 @@ def test_binding_select_path_on_cpu_tensors(cuda_lib):
 
 def _tokens(L, **over):
     a = dict(cache=16 * 1024, cbs=64 * 576, cts=576, nb=8, bt=4096, bts=4, t2s=8192, cu=12288, R=2, T=100, B=64,
-             E=576, sdt=0, ddt=0, scale=0, dst=32 * 1024, dts=576, err=0, opt=0)
+             E=576, sdt=0, ddt=0, scale=0, dst=32 * 1024, dts=576, err=0, ws=0, opt=0)
     a.update(over)
     return L.pmg_gather_tokens(a["cache"] or None, a["cbs"], a["cts"], a["nb"], a["bt"] or None, a["bts"],
                                a["t2s"] or None, a["cu"] or None, a["R"], a["T"], a["B"], a["E"], a["sdt"], a["ddt"],
-                               a["scale"] or None, a["dst"] or None, a["dts"], a["err"] or None, None, a["opt"])
+                               a["scale"] or None, a["dst"] or None, a["dts"], a["err"] or None, a["ws"] or None,
+                               None, a["opt"])
 
 
 @pytest.mark.parametrize("over,status", [
     (dict(t2s=0), 1), (dict(dst=0), 1), (dict(cache=0), 1), (dict(cu=0), 1),
-    (dict(sdt=0, ddt=1), 3), (dict(T=-1), 2), (dict(B=0), 2), (dict(dts=100), 2), (dict(opt=1), 2),
-    (dict(T=2 ** 31), 5), (dict(t2s=8194), 4), (dict(cache=16 * 1024 + 1), 4),
+    (dict(sdt=0, ddt=1), 3), (dict(T=-1), 2), (dict(B=0), 2), (dict(dts=100), 2), (dict(opt=4), 2),
+    (dict(opt=16), 2), (dict(T=2 ** 31), 5), (dict(t2s=8194), 4), (dict(cache=16 * 1024 + 1), 4),
+    (dict(ws=40 * 1024 + 8), 4),
     (dict(T=0), 0), (dict(T=0, t2s=0, dst=0), 0),
 ])
 def test_token_gather_host_validation(cuda_lib, over, status):

@@ -34,7 +34,8 @@ def token_to_seq_from_cu(cu: np.ndarray, T: int) -> np.ndarray:
     return t2s
 
 
-def _run(wl: W.Workload, t2s: np.ndarray, cu: np.ndarray, options=0, dst_row_stride=None, expect_flag=0):
+def _run(wl: W.Workload, t2s: np.ndarray, cu: np.ndarray, options=0, dst_row_stride=None, expect_flag=0,
+         workspace=False):
     T = int(t2s.shape[0])
     ed = W.ELEM_BYTES[wl.dst_dtype]
     rs = wl.entry_size if dst_row_stride is None else dst_row_stride
@@ -53,11 +54,14 @@ def _run(wl: W.Workload, t2s: np.ndarray, cu: np.ndarray, options=0, dst_row_str
     body = raw[GUARD_BYTES:GUARD_BYTES + nbytes]
     dst_full = body.view(W.TORCH_DTYPES[wl.dst_dtype]).view(T, rs)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = binding.new_workspace(dev) if workspace else None
     binding.gather_tokens(full[:, :, :wl.entry_size], dst_full[:, :wl.entry_size], wl.block_table.to(dev),
                           torch.from_numpy(t2s).to(dev), torch.from_numpy(cu).to(dev),
                           torch.tensor([wl.scale], dtype=torch.float32, device=dev), err, num_reqs=len(cu) - 1,
-                          options=options)
+                          options=options, workspace=ws)
     torch.cuda.synchronize()
+    if ws is not None:
+        assert int(ws.abs().sum().item()) == 0, f"workspace not reset: {ws.tolist()}"
     r = raw.cpu().numpy()
     assert np.all(r[:GUARD_BYTES] == FILL) and np.all(r[-GUARD_BYTES:] == FILL), "guard regions written"
     got = r[GUARD_BYTES:len(r) - GUARD_BYTES].view(W.NP_BITS[ed]).reshape(T, rs)
@@ -72,14 +76,15 @@ def _consistent(wl):
 
 
 @pytest.mark.parametrize("name", ["tiny", "60k", "skew8", "skew64_raw", "skew64_dequant"])
-@pytest.mark.parametrize("options", [0, binding.OPT_FORCE_SCALAR])
+@pytest.mark.parametrize("options", [0, binding.OPT_FORCE_SIMT, binding.OPT_FORCE_SCALAR,
+                                     binding.OPT_EARLY_METADATA])
 def test_named_workloads(name, options):
     wl = W.CONFIGS[name]()
     if wl.seq_starts is not None:  # the per-token gather has no seq_starts: positions start at 0
         wl = W.make_workload(wl.name, wl.lens, None, wl.block_size, wl.entry_size, wl.num_blocks, wl.src_dtype,
                              wl.dst_dtype, wl.scale, 77, row_stride=wl.cache.shape[2])
     t2s, cu = _consistent(wl)
-    _run(wl, t2s, cu, options=options)
+    _run(wl, t2s, cu, options=options, workspace=options == binding.OPT_EARLY_METADATA)
 
 
 PAIRS = [("bf16", "bf16"), ("fp32", "fp32"), ("u8", "u8"), ("fp8_e4m3", "bf16"), ("fp8_e4m3", "fp16"),
@@ -87,13 +92,47 @@ PAIRS = [("bf16", "bf16"), ("fp32", "fp32"), ("u8", "u8"), ("fp8_e4m3", "bf16"),
 
 
 @pytest.mark.parametrize("src,dst", PAIRS)
-@pytest.mark.parametrize("B,E,rs", [(16, 576, None), (64, 576, 640), (3, 7, None), (1, 8, 9)])
-def test_dtype_shapes(src, dst, B, E, rs):
+@pytest.mark.parametrize("B,E,rs", [(16, 576, None), (64, 576, 640), (3, 7, None), (1, 8, 9), (4, 16, None)])
+@pytest.mark.parametrize("options", [0, binding.OPT_FORCE_SIMT])
+def test_dtype_shapes(src, dst, B, E, rs, options):
     rng = np.random.default_rng(B * 100 + E)
     lens = [int(x) for x in rng.integers(0, 5 * B + 9, 7)]
     wl = W.make_workload("tok", lens, None, B, E, None, src, dst, 0.05, 31, row_stride=rs)
     t2s, cu = _consistent(wl)
+    _run(wl, t2s, cu, options=options)
+
+
+@pytest.mark.parametrize("dtypes", [("bf16", "bf16"), ("fp8_e4m3", "bf16")])
+@pytest.mark.parametrize("B", [1, 16, 64])
+def test_identity_table_runs_cross_pages(dtypes, B):
+    """Physically consecutive blocks: adjacent source rows run across page
+    boundaries and across requests, so one bulk copy spans several pages."""
+    lens = [0, 3 * B + 5, 1, 0, 7 * B, 2 * B - 1, 40]
+    need = [-(-L // B) for L in lens]
+    nb = sum(need) + 2
+    wl = W.make_workload("tok", lens, None, B, 576, nb, dtypes[0], dtypes[1], 0.05, 39)
+    bt = np.full((len(lens), max(need)), -1, np.int32)
+    pos = 1
+    for r, n in enumerate(need):
+        bt[r, :n] = np.arange(pos, pos + n, dtype=np.int32)
+        pos += n
+    wl.block_table = torch.from_numpy(bt)
+    t2s, cu = _consistent(wl)
     _run(wl, t2s, cu)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_invalid_tokens_break_runs(seed):
+    """Invalid tokens scattered through contiguous runs: the runs split around
+    them and only the valid rows are written."""
+    rng = np.random.default_rng(400 + seed)
+    wl = W.make_workload("tok", [int(x) for x in rng.integers(1, 300, 9)], None, 64, 576, None, "bf16", "bf16",
+                         1.0, 41 + seed)
+    t2s, cu = _consistent(wl)
+    t2s = t2s.copy()
+    idx = rng.choice(len(t2s), max(1, len(t2s) // 17), replace=False)
+    t2s[idx] = rng.choice([-1, 9, 100], idx.shape[0]).astype(np.int32)
+    _run(wl, t2s, cu, expect_flag=og.BAD_TOKEN, workspace=bool(seed % 2))
 
 
 def test_invalid_tokens_are_skipped_and_flagged():
@@ -127,11 +166,13 @@ def test_no_requests_every_token_flagged():
     _run(wl, np.zeros(10, np.int32), np.array([0], np.int32), expect_flag=og.BAD_TOKEN)
 
 
-def test_single_300k_tokens():
-    """300K tokens of one request through the per-token path."""
+@pytest.mark.parametrize("workspace", [False, True])
+def test_single_300k_tokens(workspace):
+    """300K tokens of one request through the per-token path (with a
+    workspace: the dynamic row split)."""
     wl = W.single_300k()
     t2s, cu = _consistent(wl)
-    _run(wl, t2s, cu)
+    _run(wl, t2s, cu, workspace=workspace)
 
 
 @pytest.mark.parametrize("T", [500_000, 1_000_000])
