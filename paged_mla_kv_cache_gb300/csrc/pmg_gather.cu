@@ -98,6 +98,7 @@ struct Params {
   int32_t* sched;         // work-claim counter in the caller's workspace, or null (static split)
   const int32_t* gate;    // large batches: non-zero when cu_seq_lens failed validation (write nothing)
   int32_t early;          // plan and first block ids before the previous grid completes (caller's promise)
+  int32_t spec;           // plan and first batch before the previous grid completes, checked after it
   const int32_t* t2s;     // per-token gather: request of each output row (token mode)
   int32_t token_mode;     // 1: rows [0, T) map through t2s instead of the page plan
   int32_t sched_static_pct;  // dynamic mode: share of rows split statically up front
@@ -138,9 +139,12 @@ __device__ __forceinline__ uint64_t evict_last_policy() {
   return pol;
 }
 
+// Loads of metadata are coherent at GPU scope (never served from a stale L1
+// line): a speculative plan reads it before the previous grid is known to be
+// done, and the check after the wait must see the final values.
 __device__ __forceinline__ int32_t ld_meta(const int32_t* ptr, uint64_t pol) {
   int32_t v;
-  asm volatile("ld.global.nc.L2::cache_hint.b32 %0, [%1], %2;" : "=r"(v) : "l"(ptr), "l"(pol));
+  asm volatile("ld.relaxed.gpu.global.L2::cache_hint.b32 %0, [%1], %2;" : "=r"(v) : "l"(ptr), "l"(pol));
   return v;
 }
 
@@ -195,6 +199,11 @@ __device__ __forceinline__ PlanView plan_view(uint8_t* base, const Params& p) {
   return v;
 }
 
+// Bytes of one plan in shared memory (ob, st and P back to back).
+__device__ __forceinline__ size_t plan_bytes(const Params& p) {
+  return (static_cast<size_t>(3) * p.R + 2) * sizeof(int32_t);
+}
+
 // Pages of request r: the logical blocks its source range [s, s + len) touches
 // (0 for len == 0 or a negative start). With 0 <= s <= 2^31-1 and
 // 1 <= len <= 2^31-1, s + len - 1 < 2^32, so 32-bit unsigned division is exact.
@@ -217,7 +226,7 @@ __device__ __forceinline__ int32_t request_pages(const PlanView& v, int r, int B
 constexpr int kWarpPlanMaxReqs = 256;
 
 template <bool kWarp>
-__device__ int build_plan(const Params& p, const PlanView& v, bool report_flags) {
+__device__ int build_plan(const Params& p, const PlanView& v, bool report_flags, int* flags_out = nullptr) {
   __shared__ int32_t warp_sums[32];
   __shared__ int32_t total_pages;
   const int tid = kWarp ? static_cast<int>(threadIdx.x & 31) : static_cast<int>(threadIdx.x);
@@ -247,6 +256,7 @@ __device__ int build_plan(const Params& p, const PlanView& v, bool report_flags)
   const bool any_bad = kWarp ? (__syncwarp(), __any_sync(0xffffffffu, bad)) : __syncthreads_or(bad);
   if (any_bad) {
     if (report_flags && tid == 0) set_flag(p, PMG_FLAG_CU_ORDER);
+    if (flags_out != nullptr) *flags_out = PMG_FLAG_CU_ORDER;
     return -1;
   }
 
@@ -296,6 +306,7 @@ __device__ int build_plan(const Params& p, const PlanView& v, bool report_flags)
   if (tid == 0) v.P[R] = total;
   const bool any_bad_start = kWarp ? (__syncwarp(), __any_sync(0xffffffffu, bad_start)) : __syncthreads_or(bad_start);
   if (any_bad_start && report_flags && tid == 0) set_flag(p, PMG_FLAG_SEQ_START);
+  if (flags_out != nullptr) *flags_out = any_bad_start ? PMG_FLAG_SEQ_START : 0;
   return total;
 }
 
@@ -402,11 +413,19 @@ struct Segment {
   int32_t pad;
 };
 
+// What a speculative resolution read and would have reported.
+struct SpecRead {
+  int bits;      // flag bits it would set
+  int64_t idx;   // block-table element it read, or -1
+  int32_t phys;  // the value read there
+};
+
 // Resolves task t for a CTA owning rows [row0, row1). Returns false when the
 // task starts at or past row1 (tasks are ordered by output row, so every
-// later task does too).
+// later task does too). With rec, flag bits and the block-table read are
+// recorded there instead of reported.
 __device__ __forceinline__ bool resolve_segment(const Params& p, const PlanView& v, int32_t t, int32_t num_tasks,
-                                                int32_t row0, int32_t row1, Segment& seg) {
+                                                int32_t row0, int32_t row1, Segment& seg, SpecRead* rec = nullptr) {
   seg.nrows = 0;
   seg.src = 0;
   seg.dst = 0;
@@ -418,12 +437,19 @@ __device__ __forceinline__ bool resolve_segment(const Params& p, const PlanView&
   const int64_t hi = task_end < row1 ? task_end : row1;
   if (hi <= lo) return true;
   if (k.logical_block >= p.bt_stride) {
-    set_flag(p, PMG_FLAG_LOGICAL_BLOCK);
+    if (rec != nullptr) rec->bits |= PMG_FLAG_LOGICAL_BLOCK;
+    else set_flag(p, PMG_FLAG_LOGICAL_BLOCK);
     return true;
   }
-  const int64_t phys = ld_meta(p.bt + static_cast<int64_t>(k.req) * p.bt_stride + k.logical_block, evict_last_policy());
+  const int64_t idx = static_cast<int64_t>(k.req) * p.bt_stride + k.logical_block;
+  const int64_t phys = ld_meta(p.bt + idx, evict_last_policy());
+  if (rec != nullptr) {
+    rec->idx = idx;
+    rec->phys = static_cast<int32_t>(phys);
+  }
   if (phys < 0 || phys >= p.num_blocks) {
-    set_flag(p, PMG_FLAG_PHYS_BLOCK);
+    if (rec != nullptr) rec->bits |= PMG_FLAG_PHYS_BLOCK;
+    else set_flag(p, PMG_FLAG_PHYS_BLOCK);
     return true;
   }
   const int64_t slot = k.begin + (lo - k.out);
@@ -512,6 +538,7 @@ struct Chunk {
   int64_t src;
   int64_t dst;
   int32_t nrows;
+  int32_t tentative;  // from the speculative first batch: store only once it is confirmed
 };
 
 // Walks a segment table chunk by chunk (at most rows_per_stage rows each).
@@ -679,6 +706,8 @@ struct SegQueue {
   int32_t count[kSegBufs];  // -1: no more work
   uint64_t full[kSegBufs];
   uint64_t empty[kSegBufs];
+  int32_t tentative;  // batch 0 is the speculative first batch
+  int32_t verdict;    // for it: 0 pending, 1 confirmed, 2 withdrawn
 };
 
 __device__ __forceinline__ void segq_init(SegQueue& q) {
@@ -686,15 +715,87 @@ __device__ __forceinline__ void segq_init(SegQueue& q) {
     mbar_init(&q.full[b], 1);
     mbar_init(&q.empty[b], 1);
   }
+  q.tentative = 0;
+  q.verdict = 0;
+}
+
+// Verdict on the speculative first batch: 1 confirmed, 0 withdrawn, -1 the
+// bounded wait for it ran out.
+__device__ __forceinline__ int spec_verdict(const SegQueue& q) {
+  const volatile int32_t* vp = &q.verdict;
+  int32_t v = *vp;
+  if (v == 0) {
+    const uint64_t t0 = global_ns();
+    while ((v = *vp) == 0) {
+      if (global_ns() - t0 > kWaitLimitNs) return -1;
+    }
+  }
+  return v == 1 ? 1 : 0;
 }
 
 // The scheduler warp: takes items (its static one, then claimed ones) and
 // resolves each into batches of up to 32 segments, one task per lane (map,
 // block-table read, bounds checks). Returns false on a timeout.
-__device__ bool run_scheduler(const Params& p, const PlanView& v, int32_t num_tasks, SegQueue& q) {
+//
+// Speculative start (p.spec, warp plans only): before the previous grid is
+// known to be done, the warp plans into the spare area sv and resolves the
+// first batch of its static item, reporting nothing, and publishes that batch
+// marked tentative, so that the producer can start its loads the moment the
+// wait returns (loads only read the cache, at addresses checked in bounds).
+// After the wait it reads the block-table entries again and plans again into
+// v from the inputs as they now are: if both plans and every entry agree, the
+// batch is what a plan after the wait would have produced and is confirmed;
+// otherwise it is withdrawn (its chunks are dropped unstored) and the item is
+// resolved again from the start.
+__device__ bool run_scheduler(const Params& p, const PlanView& v, const PlanView& sv, int32_t num_tasks,
+                              SegQueue& q) {
   const int lane = threadIdx.x & 31;
   uint32_t uses = 0;
   uint32_t k = blockIdx.x;
+  // first item only: -1 resolve from its first task, -2 already done, else resume at this task
+  int32_t resume_t = -1;
+  if (p.spec) {
+    int plan_flags = 0;
+    const int32_t sn = build_plan<true>(p, sv, false, &plan_flags);
+    SpecRead rd{0, -1, 0};
+    Segment seg{};
+    int32_t t0 = 0;
+    int n = 0;
+    bool ok = false;
+    if (sn > 0 && plan_flags == 0) {
+      const Items si = make_items(sv, p);
+      uint32_t r0 = 0, r1 = 0;
+      if (k < si.n) item_rows(si, k, r0, r1);
+      if (r0 < r1) {
+        t0 = first_task_for_row(sv, p.R, p.B, r0);
+        const bool act = resolve_segment(p, sv, t0 + lane, sn, static_cast<int32_t>(r0), static_cast<int32_t>(r1),
+                                         seg, &rd);
+        n = __popc(__ballot_sync(0xffffffffu, act));
+        ok = n > 0 && __all_sync(0xffffffffu, rd.bits == 0);
+      }
+    }
+    if (ok) {
+      q.seg[0][lane] = seg;
+      if (lane == 0) {
+        q.count[0] = n;
+        q.tentative = 1;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&q.full[0]);
+      uses = 1;
+    }
+    pdl_wait();
+    const int32_t phys_now = (ok && rd.idx >= 0) ? ld_meta(p.bt + rd.idx, evict_last_policy()) : 0;
+    num_tasks = build_plan<true>(p, v, blockIdx.x == 0);
+    if (ok) {
+      bool same = num_tasks == sn && phys_now == rd.phys;
+      const int words = 3 * p.R + 2;  // ob, st and P are contiguous
+      for (int i = lane; i < words; i += 32) same = same && v.ob[i] == sv.ob[i];
+      const bool valid = __all_sync(0xffffffffu, same);
+      if (lane == 0) *reinterpret_cast<volatile int32_t*>(&q.verdict) = valid ? 1 : 2;
+      if (valid) resume_t = n < kSegCap ? -2 : t0 + kSegCap;
+    }
+  }
   Items its{};
   bool have = false;
   if (num_tasks > 0) {
@@ -749,8 +850,8 @@ __device__ bool run_scheduler(const Params& p, const PlanView& v, int32_t num_ta
           ++uses;
         }
       }
-    } else if (r0 < r1) {
-      int32_t t = first_task_for_row(v, p.R, p.B, r0);
+    } else if (r0 < r1 && resume_t != -2) {
+      int32_t t = resume_t >= 0 ? resume_t : first_task_for_row(v, p.R, p.B, r0);
       for (;;) {
         Segment seg;
         const bool act = resolve_segment(p, v, t + lane, num_tasks, static_cast<int32_t>(r0),
@@ -768,6 +869,7 @@ __device__ bool run_scheduler(const Params& p, const PlanView& v, int32_t num_ta
         t += kSegCap;
       }
     }
+    resume_t = -1;
     if (!waited) {
       pdl_wait();
       waited = true;
@@ -801,12 +903,16 @@ struct SegReader {
   int n;
   ChunkIter it;
   bool end;
+  int32_t tentative;
   // 1: a chunk; 0: none ready yet (only when block is false); -1: no more work;
   // -2: a bounded wait ran out
   __device__ __forceinline__ int next(SegQueue& q, const Params& p, Chunk& c, bool block) {
     for (;;) {
       if (cur >= 0) {
-        if (it.next(q.seg[cur], n, p.rows_per_stage, p, c)) return 1;
+        if (it.next(q.seg[cur], n, p.rows_per_stage, p, c)) {
+          c.tentative = tentative;
+          return 1;
+        }
         mbar_arrive(&q.empty[cur]);  // chunk descriptors are copied out: the batch is free
         ++uses;
         cur = -1;
@@ -827,6 +933,7 @@ struct SegReader {
       }
       cur = b;
       it = ChunkIter{0, 0};
+      tentative = (uses == 0 && q.tentative) ? 1 : 0;
     }
   }
 };
@@ -852,9 +959,11 @@ __global__ void __launch_bounds__(kBulkThreads) gather_bulk_kernel(const __grid_
   __shared__ Chunk stage_chunk[kMaxStages];
   __shared__ __align__(8) SegQueue q;
 
-  // layout: [stages][plan]; stage buffers first keeps them 128-byte aligned
+  // layout: [stages][plan][speculative plan]; stage buffers first keeps them 128-byte aligned
   uint8_t* stage_base = smem;
   const PlanView v = plan_view(smem + static_cast<size_t>(p.stages) * p.stage_bytes, p);
+  // the speculative plan's area follows the plan (allocated only with p.spec)
+  const PlanView sv = plan_view(smem + static_cast<size_t>(p.stages) * p.stage_bytes + plan_bytes(p), p);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -867,10 +976,10 @@ __global__ void __launch_bounds__(kBulkThreads) gather_bulk_kernel(const __grid_
   }
   prefetch_metadata(p);
   pdl_trigger();
-  // With early metadata the scheduler warp plans and resolves its first batch
-  // while the previous grid may still run; every read of the cache, scale or
-  // workspace and every write of dst comes after the wait.
-  const bool early = p.early != 0;
+  // With early metadata or speculation the scheduler warp plans and resolves
+  // its first batch while the previous grid may still run; every read of the
+  // cache, scale or workspace and every write of dst comes after the wait.
+  const bool early = p.early != 0 || p.spec != 0;
   if (!early) pdl_wait();
   if (p.gate != nullptr && *reinterpret_cast<const volatile int32_t*>(p.gate) != 0) return;
   __syncthreads();
@@ -885,14 +994,14 @@ __global__ void __launch_bounds__(kBulkThreads) gather_bulk_kernel(const __grid_
 
   if (warp == 1) {
     if (p.token_mode) num_tasks = 1;
-    else if (warp_plan) num_tasks = build_plan<true>(p, v, blockIdx.x == 0);
-    if (!run_scheduler(p, v, num_tasks, q)) set_flag(p, PMG_FLAG_TIMEOUT);
+    else if (warp_plan && !p.spec) num_tasks = build_plan<true>(p, v, blockIdx.x == 0);
+    if (!run_scheduler(p, v, sv, num_tasks, q)) set_flag(p, PMG_FLAG_TIMEOUT);
   } else if (tid == 0) {
     if (early) pdl_wait();
     const uint64_t pol = evict_first_policy();
     const uint32_t row_bytes = static_cast<uint32_t>(p.row_src_bytes);
     const uint32_t S = static_cast<uint32_t>(p.stages);
-    SegReader rd{0, -1, 0, ChunkIter{0, 0}, false};
+    SegReader rd{0, -1, 0, ChunkIter{0, 0}, false, 0};
     uint32_t loads = 0, stores = 0;
     bool gen_done = false;
     bool ok = true;
@@ -926,6 +1035,17 @@ __global__ void __launch_bounds__(kBulkThreads) gather_bulk_kernel(const __grid_
         break;
       }
       const Chunk c = stage_chunk[s];
+      if (c.tentative) {
+        const int vr = spec_verdict(q);
+        if (vr != 1) {
+          // withdrawn (or no verdict in time): drop the chunk; an empty group
+          // keeps the count of bulk groups in step with `stores`
+          if (vr < 0) set_flag(p, PMG_FLAG_TIMEOUT);
+          bulk_commit();
+          ++stores;
+          continue;
+        }
+      }
       const uint8_t* buf = stage_base + static_cast<size_t>(s) * p.stage_bytes;
       if (p.dst_dense) {
         bulk_store(p.dst + c.dst, buf, static_cast<uint32_t>(c.nrows) * row_bytes);
@@ -1214,6 +1334,8 @@ __global__ void __launch_bounds__(kCvtThreads) gather_tma_convert_kernel(const _
 
   uint8_t* stage_base = smem;
   const PlanView v = plan_view(smem + static_cast<size_t>(p.stages) * p.stage_bytes, p);
+  // the speculative plan's area follows the plan (allocated only with p.spec)
+  const PlanView sv = plan_view(smem + static_cast<size_t>(p.stages) * p.stage_bytes + plan_bytes(p), p);
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
@@ -1229,10 +1351,10 @@ __global__ void __launch_bounds__(kCvtThreads) gather_tma_convert_kernel(const _
   }
   prefetch_metadata(p);
   pdl_trigger();
-  // With early metadata the scheduler warp plans and resolves its first batch
-  // while the previous grid may still run; every read of the cache, scale or
-  // workspace and every write of dst comes after the wait.
-  const bool early = p.early != 0;
+  // With early metadata or speculation the scheduler warp plans and resolves
+  // its first batch while the previous grid may still run; every read of the
+  // cache, scale or workspace and every write of dst comes after the wait.
+  const bool early = p.early != 0 || p.spec != 0;
   if (!early) pdl_wait();
   if (p.gate != nullptr && *reinterpret_cast<const volatile int32_t*>(p.gate) != 0) return;
   __syncthreads();
@@ -1247,15 +1369,15 @@ __global__ void __launch_bounds__(kCvtThreads) gather_tma_convert_kernel(const _
 
   if (warp == kCvtWarps + 1) {
     if (p.token_mode) num_tasks = 1;
-    else if (warp_plan) num_tasks = build_plan<true>(p, v, blockIdx.x == 0);
-    if (!run_scheduler(p, v, num_tasks, q)) set_flag(p, PMG_FLAG_TIMEOUT);
+    else if (warp_plan && !p.spec) num_tasks = build_plan<true>(p, v, blockIdx.x == 0);
+    if (!run_scheduler(p, v, sv, num_tasks, q)) set_flag(p, PMG_FLAG_TIMEOUT);
   } else if (warp == kCvtWarps) {
     // producer: one lane issues the bulk loads, up to p.stages chunks ahead
     if (lane == 0) {
       if (early) pdl_wait();
       const uint64_t pol = evict_first_policy();
       const uint32_t S = static_cast<uint32_t>(p.stages);
-      SegReader rd{0, -1, 0, ChunkIter{0, 0}, false};
+      SegReader rd{0, -1, 0, ChunkIter{0, 0}, false, 0};
       for (uint32_t g = 0;; ++g) {
         Chunk c;
         const int r = rd.next(q, p, c, true);
@@ -1293,6 +1415,16 @@ __global__ void __launch_bounds__(kCvtThreads) gather_tma_convert_kernel(const _
       }
       const Chunk c = stage_chunk[s];
       if (c.nrows == 0) break;
+      if (c.tentative) {
+        const int vr = spec_verdict(q);
+        if (vr != 1) {
+          // withdrawn (or no verdict in time): drop the chunk unconverted
+          if (vr < 0 && tid == 0) set_flag(p, PMG_FLAG_TIMEOUT);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty_bar[s]);
+          continue;
+        }
+      }
       const uint8_t* in = stage_base + static_cast<size_t>(s) * p.stage_bytes;
       const uint32_t units = static_cast<uint32_t>(c.nrows) * upr;
       uint8_t* out = p.dst + c.dst;
@@ -1553,6 +1685,12 @@ int sched_static_pct() {
   static const int v = env_int("PMG_SCHED_STATIC_PCT", 25, 0, 100);
   return v;
 }
+// Speculative start of the TMA paths (PMG_SPEC=0 turns it off).
+bool use_spec() {
+  static const int v = env_int("PMG_SPEC", 1, 0, 1);
+  return v != 0;
+}
+
 int sched_min_rows() {
   static const int v = env_int("PMG_SCHED_MIN_ROWS", 128, 1, 1 << 30);
   return v;
@@ -1676,6 +1814,9 @@ int make_plan(const void* cache, int64_t cbs, int64_t cts, int64_t num_blocks, c
   q.sched = workspace;
   // large batches read a verdict from the workspace first: no early start there
   q.early = ((options & PMG_OPT_EARLY_METADATA) && R <= PMG_MAX_REQS_PLAN) ? 1 : 0;
+  // without the promise, small batches still plan before the wait and check
+  // the plan after it (the TMA paths; the SIMT kernels ignore the field)
+  q.spec = (!q.early && R <= kWarpPlanMaxReqs && use_spec()) ? 1 : 0;
   q.sched_static_pct = sched_static_pct();
   q.sched_min_rows = sched_min_rows();
   out.conv = conv;
@@ -1904,7 +2045,8 @@ int launch_one(const Plan& pl, cudaStream_t stream) {
     KernelFn k = copy ? gather_bulk_kernel : tma_convert_kernel_for(pl.conv);
     if (k == nullptr) return PMG_ERR_UNSUPPORTED;
     const int threads = copy ? kBulkThreads : kCvtThreads;
-    const size_t smem = static_cast<size_t>(q.stages) * q.stage_bytes + (q.token_mode ? 0 : host_plan_bytes(q.R));
+    const size_t plans = q.token_mode ? 0 : (q.spec ? 2 : 1) * host_plan_bytes(q.R);
+    const size_t smem = static_cast<size_t>(q.stages) * q.stage_bytes + plans;
     int per_sm = 0;
     if (ctas_per_sm(k, threads, smem, &per_sm) != PMG_OK) return PMG_ERR_CUDA;
     if (per_sm < 1) return PMG_ERR_UNSUPPORTED;
@@ -2100,6 +2242,7 @@ int pmg_gather_tokens(const void* cache, int64_t cache_block_stride, int64_t cac
       pl.prm.R = num_reqs;
       pl.prm.t2s = token_to_seq;
       pl.prm.token_mode = 1;
+      pl.prm.spec = 0;
       return launch_one(pl, static_cast<cudaStream_t>(stream));
     }
   }

@@ -1,0 +1,97 @@
+"""The speculative start of the TMA paths, under real overlap.
+
+Without the caller's early-metadata promise, a small batch still plans and
+resolves its first batch before the previous grid in the stream is known to be
+done, and checks both against the inputs as they are after the wait. Here the
+previous grid is itself a gather whose output IS the next gather's
+cu_seq_lens and block table: it starts (programmatic dependent launch) while
+the first one still writes them, so its speculative reads can see the old
+tables. Old and new tables are both valid, so every speculative read stays in
+bounds; the result must equal the oracle on the NEW tables, bit for bit, on
+every repetition, whichever way each race went.
+
+Source for the expected output: "MLA cache gather scheduled per logical page"
+(prhub.com.cn, vllm PR #51739), section "关键源码片段", the per-token
+expected output of test_cp_gather_cache_mla_large_uneven_sequences.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import gather as og
+from paged_mla_kv_cache_gb300 import binding
+from paged_mla_kv_cache_gb300 import workloads as W
+
+from gpu_helpers import assert_same
+
+pytestmark = pytest.mark.gpu
+
+R, STRIDE, B, NB = 3, 16, 16, 64
+META_INTS = 64  # cu at [0, R], block table at [16, 16 + R * STRIDE)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(cuda_lib):
+    if not torch.cuda.is_available():
+        pytest.fail("a GPU test ran without a CUDA device")
+    return cuda_lib
+
+
+def _meta(rng, lens):
+    """A valid (cu, block table) pair packed into META_INTS int32."""
+    m = np.zeros(META_INTS, np.int32)
+    m[:R + 1] = np.concatenate([[0], np.cumsum(lens)])
+    perm = rng.permutation(NB).astype(np.int32)
+    m[16:16 + R * STRIDE] = perm[:R * STRIDE]
+    return m
+
+
+def _oracle(cache_bits, meta, E, src, dst_dtype, scale, T):
+    cu = meta[:R + 1].copy()
+    bt = meta[16:16 + R * STRIDE].reshape(R, STRIDE).copy()
+    ed = W.ELEM_BYTES[dst_dtype]
+    want = np.full((T, E * ed), 0xA5, np.uint8).view(W.NP_BITS[ed])
+    flag = og.gather(cache_bits, bt, cu, None, R, T, B, E, src, dst_dtype, scale, want)
+    return want, flag
+
+
+@pytest.mark.parametrize("src,dst", [("bf16", "bf16"), ("fp8_e4m3", "bf16")])
+@pytest.mark.parametrize("same", [False, True])
+def test_metadata_written_by_the_previous_grid(src, dst, same):
+    dev = "cuda:0"
+    E = 64
+    rng = np.random.default_rng(71 if same else 72)
+    # the gathered cache: NB blocks of B slots
+    wl = W.make_workload("spec", [B * NB], None, B, E, NB, src, dst, 0.05, 73)
+    cache = wl.cache.to(dev)
+    cache_bits = W.tensor_bits(wl.cache)
+    scale = torch.tensor([wl.scale], dtype=torch.float32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    # the first gather copies one fp32 row of META_INTS elements: the tables
+    one_bt = torch.zeros(1, 1, dtype=torch.int32, device=dev)
+    one_cu = torch.tensor([0, 1], dtype=torch.int32, device=dev)
+    meta = torch.empty(META_INTS, dtype=torch.int32, device=dev)
+    cu_dev = meta[:R + 1]
+    bt_dev = meta[16:16 + R * STRIDE].view(R, STRIDE)
+    for it in range(24):
+        lens_new = [int(x) for x in rng.integers(1, 5 * B, R)]
+        lens_old = [int(x) for x in rng.integers(1, 5 * B, R)]
+        new = _meta(rng, lens_new)
+        old = new.copy() if same else _meta(rng, lens_old)
+        T = int(max(new[R], old[R]))
+        src_row = torch.from_numpy(new.view(np.float32).copy()).to(dev).view(1, 1, META_INTS)
+        meta.copy_(torch.from_numpy(old))
+        out = torch.full((T, E), 0, dtype=W.TORCH_DTYPES[dst], device=dev)
+        out.view(torch.uint8).fill_(0xA5)
+        err.zero_()
+        torch.cuda.synchronize()
+        # queue both behind a busy kernel so that they start back to back
+        torch.cuda._sleep(200_000)
+        binding.gather(src_row, meta.view(torch.float32).view(1, META_INTS), one_bt, one_cu, error_flag=err)
+        binding.gather(cache, out, bt_dev, cu_dev, None, scale, err, num_reqs=R)
+        torch.cuda.synchronize()
+        assert np.array_equal(meta.cpu().numpy(), new)
+        want, flag = _oracle(cache_bits, new, E, src, dst, wl.scale, T)
+        got = out.cpu().view(torch.uint8).numpy().view(W.NP_BITS[W.ELEM_BYTES[dst]]).reshape(T, E)
+        assert int(err.item()) == flag == 0
+        assert_same(got, want, dst, src != dst)
