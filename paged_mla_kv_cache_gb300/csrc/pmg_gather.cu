@@ -642,9 +642,18 @@ __device__ __forceinline__ void item_rows(const Items& it, uint32_t k, uint32_t&
 // offset of the row, or -1 (flag bits in `bits`; tokens at or past t_end set none).
 constexpr int kTokGroup = 4;
 
+// What the resolution of one token read (for the speculative start's check).
+struct TokRead {
+  int32_t b;    // token_to_seq[t] as read
+  int32_t c0;   // cu_seq_lens[b] and [b + 1], when b was in range
+  int32_t c1;
+  int32_t phys; // the block-table entry read, at idx (or idx = -1)
+  int64_t idx;
+};
+
 template <int N>
 __device__ __forceinline__ void resolve_tokens(const Params& p, uint32_t t_first, uint32_t t_end, int64_t (&src)[N],
-                                               int& bits) {
+                                               int& bits, TokRead (&rec)[N]) {
   const uint64_t keep = evict_last_policy();
   int32_t b[N];
 #pragma unroll
@@ -652,6 +661,7 @@ __device__ __forceinline__ void resolve_tokens(const Params& p, uint32_t t_first
     const uint32_t t = t_first + 32u * j;
     src[j] = -1;
     b[j] = t < t_end ? ld_meta(p.t2s + t, keep) : -1;
+    rec[j] = TokRead{b[j], 0, 0, 0, -1};
     if (t < t_end && (b[j] < 0 || b[j] >= p.R)) {
       bits |= PMG_FLAG_TOKEN;
       b[j] = -1;
@@ -662,6 +672,8 @@ __device__ __forceinline__ void resolve_tokens(const Params& p, uint32_t t_first
   for (int j = 0; j < N; ++j) {
     c0[j] = b[j] >= 0 ? ld_meta(p.cu + b[j], keep) : 0;
     c1[j] = b[j] >= 0 ? ld_meta(p.cu + b[j] + 1, keep) : 0;
+    rec[j].c0 = c0[j];
+    rec[j].c1 = c1[j];
   }
   int32_t phys[N];
   uint32_t off[N];
@@ -684,7 +696,9 @@ __device__ __forceinline__ void resolve_tokens(const Params& p, uint32_t t_first
       b[j] = -1;
       continue;
     }
-    phys[j] = ld_meta(p.bt + static_cast<int64_t>(b[j]) * p.bt_stride + lb, keep);
+    rec[j].idx = static_cast<int64_t>(b[j]) * p.bt_stride + lb;
+    phys[j] = ld_meta(p.bt + rec[j].idx, keep);
+    rec[j].phys = phys[j];
   }
 #pragma unroll
   for (int j = 0; j < N; ++j) {
@@ -695,6 +709,19 @@ __device__ __forceinline__ void resolve_tokens(const Params& p, uint32_t t_first
     }
     src[j] = static_cast<int64_t>(phys[j]) * p.blk_stride_b + static_cast<int64_t>(off[j]) * p.tok_stride_b;
   }
+}
+
+// Whether the token's inputs still hold what `r` recorded (token t < t_end).
+// The loads go to the recorded addresses and are issued together.
+__device__ __forceinline__ bool token_unchanged(const Params& p, uint32_t t, uint32_t t_end, const TokRead& r) {
+  if (t >= t_end) return true;
+  const uint64_t keep = evict_last_policy();
+  const bool in = r.b >= 0 && r.b < p.R;
+  const int32_t b = ld_meta(p.t2s + t, keep);
+  const int32_t c0 = in ? ld_meta(p.cu + r.b, keep) : 0;
+  const int32_t c1 = in ? ld_meta(p.cu + r.b + 1, keep) : 0;
+  const int32_t ph = r.idx >= 0 ? ld_meta(p.bt + r.idx, keep) : 0;
+  return b == r.b && c0 == r.c0 && c1 == r.c1 && ph == (r.idx >= 0 ? r.phys : 0);
 }
 
 // Segment batches handed from the scheduler warp to the producer thread.
@@ -733,6 +760,41 @@ __device__ __forceinline__ int spec_verdict(const SegQueue& q) {
   return v == 1 ? 1 : 0;
 }
 
+// Publishes the 32 tokens t0 + lane (row source offset src, -1 for none) as
+// one batch: consecutive lanes whose source rows are one slot apart form one
+// segment. Returns the number of segments (0: nothing to publish) or -1 when
+// the bounded wait for a free batch ran out.
+__device__ __forceinline__ int publish_tokens(const Params& p, SegQueue& q, uint32_t& uses, uint32_t t0,
+                                              int64_t src) {
+  const int lane = threadIdx.x & 31;
+  const int64_t prev = __shfl_up_sync(0xffffffffu, src, 1);
+  const bool valid = src >= 0;
+  const bool cont = lane > 0 && valid && prev >= 0 && src == prev + p.tok_stride_b;
+  const bool start = valid && !cont;
+  const uint32_t starts = __ballot_sync(0xffffffffu, start);
+  const uint32_t breaks = __ballot_sync(0xffffffffu, !cont);
+  const int n = __popc(starts);
+  if (n == 0) return 0;
+  const int b = static_cast<int>(uses % kSegBufs);
+  if (uses >= kSegBufs && !mbar_wait_bounded(&q.empty[b], ((uses / kSegBufs) - 1u) & 1u)) return -1;
+  if (start) {
+    // the segment runs to the next lane that starts one or is empty
+    const uint32_t after = lane == 31 ? 0u : (breaks & (0xffffffffu << (lane + 1)));
+    const int next = after ? __ffs(after) - 1 : 32;
+    Segment seg;
+    seg.src = src;
+    seg.dst = static_cast<int64_t>(t0 + static_cast<uint32_t>(lane)) * p.dst_stride_b;
+    seg.nrows = next - lane;
+    seg.pad = 0;
+    q.seg[b][__popc(starts & ((1u << lane) - 1u))] = seg;
+  }
+  if (lane == 0) q.count[b] = n;
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&q.full[b]);
+  ++uses;
+  return n;
+}
+
 // The scheduler warp: takes items (its static one, then claimed ones) and
 // resolves each into batches of up to 32 segments, one task per lane (map,
 // block-table read, bounds checks). Returns false on a timeout.
@@ -754,7 +816,29 @@ __device__ bool run_scheduler(const Params& p, const PlanView& v, const PlanView
   uint32_t k = blockIdx.x;
   // first item only: -1 resolve from its first task, -2 already done, else resume at this task
   int32_t resume_t = -1;
-  if (p.spec) {
+  if (p.spec && p.token_mode) {
+    // the first 32 tokens of the static item, checked after the wait by
+    // reading every input they depended on again
+    const Items si = make_items(v, p);
+    uint32_t r0 = 0, r1 = 0;
+    if (k < si.n) item_rows(si, k, r0, r1);
+    int64_t src[1] = {-1};
+    TokRead rec[1] = {TokRead{0, 0, 0, 0, -1}};
+    int bits = 0;
+    if (r0 < r1) resolve_tokens<1>(p, r0 + static_cast<uint32_t>(lane), r1, src, bits, rec);
+    const bool ok = r0 < r1 && __all_sync(0xffffffffu, bits == 0) && __any_sync(0xffffffffu, src[0] >= 0);
+    if (ok) {
+      if (lane == 0) q.tentative = 1;
+      (void)publish_tokens(p, q, uses, r0, src[0]);  // the first batch: no wait
+    }
+    pdl_wait();
+    if (ok) {
+      const bool same = token_unchanged(p, r0 + static_cast<uint32_t>(lane), r1, rec[0]);
+      const bool valid = __all_sync(0xffffffffu, same);
+      if (lane == 0) *reinterpret_cast<volatile int32_t*>(&q.verdict) = valid ? 1 : 2;
+      if (valid) resume_t = r0 + 32u < r1 ? static_cast<int32_t>(r0 + 32u) : -2;
+    }
+  } else if (p.spec) {
     int plan_flags = 0;
     const int32_t sn = build_plan<true>(p, sv, false, &plan_flags);
     SpecRead rd{0, -1, 0};
@@ -811,44 +895,17 @@ __device__ bool run_scheduler(const Params& p, const PlanView& v, const PlanView
     if (its.dynamic && lane == 0 && waited) claimed = gridDim.x + atomicAdd(reinterpret_cast<unsigned*>(p.sched), 1u);
     uint32_t r0, r1;
     item_rows(its, k, r0, r1);
-    if (r0 < r1 && p.token_mode) {
-      // 32 tokens per batch, one per lane; consecutive lanes whose source rows
-      // are one slot apart form one segment
-      for (uint32_t g0 = r0; g0 < r1; g0 += 32u * kTokGroup) {
+    if (r0 < r1 && p.token_mode && resume_t != -2) {
+      // 32 tokens per batch, one per lane, kTokGroup batches resolved together
+      for (uint32_t g0 = resume_t >= 0 ? static_cast<uint32_t>(resume_t) : r0; g0 < r1; g0 += 32u * kTokGroup) {
         int64_t srcs[kTokGroup];
+        TokRead rec[kTokGroup];
         int bits = 0;
-        resolve_tokens<kTokGroup>(p, g0 + static_cast<uint32_t>(lane), r1, srcs, bits);
+        resolve_tokens<kTokGroup>(p, g0 + static_cast<uint32_t>(lane), r1, srcs, bits, rec);
         if (bits != 0) set_flag(p, bits);
 #pragma unroll
-        for (int j = 0; j < kTokGroup; ++j) {
-          const uint32_t t = g0 + 32u * j + static_cast<uint32_t>(lane);
-          const int64_t src = srcs[j];
-          const int64_t prev = __shfl_up_sync(0xffffffffu, src, 1);
-          const bool valid = src >= 0;
-          const bool cont = lane > 0 && valid && prev >= 0 && src == prev + p.tok_stride_b;
-          const bool start = valid && !cont;
-          const uint32_t starts = __ballot_sync(0xffffffffu, start);
-          const uint32_t breaks = __ballot_sync(0xffffffffu, !cont);
-          const int n = __popc(starts);
-          if (n == 0) continue;
-          const int b = static_cast<int>(uses % kSegBufs);
-          if (uses >= kSegBufs && !mbar_wait_bounded(&q.empty[b], ((uses / kSegBufs) - 1u) & 1u)) return false;
-          if (start) {
-            // the segment runs to the next lane that starts one or is empty
-            const uint32_t after = lane == 31 ? 0u : (breaks & (0xffffffffu << (lane + 1)));
-            const int next = after ? __ffs(after) - 1 : 32;
-            Segment seg;
-            seg.src = src;
-            seg.dst = static_cast<int64_t>(t) * p.dst_stride_b;
-            seg.nrows = next - lane;
-            seg.pad = 0;
-            q.seg[b][__popc(starts & ((1u << lane) - 1u))] = seg;
-          }
-          if (lane == 0) q.count[b] = n;
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&q.full[b]);
-          ++uses;
-        }
+        for (int j = 0; j < kTokGroup; ++j)
+          if (publish_tokens(p, q, uses, g0 + 32u * j, srcs[j]) < 0) return false;
       }
     } else if (r0 < r1 && resume_t != -2) {
       int32_t t = resume_t >= 0 ? resume_t : first_task_for_row(v, p.R, p.B, r0);
@@ -1662,11 +1719,13 @@ int bulk_stage_target_bytes() {
 }
 
 // Target bytes (of source rows) of one stage of the converting TMA ring;
-// PMG_CVT_STAGE_KB (4..48) overrides the default for tuning sweeps.
+// PMG_CVT_STAGE_KB (4..48) overrides the default for tuning sweeps. 10 KB
+// stages leave room for five CTAs per SM, which measured best for fp8 rows
+// of 576 bytes (more CTAs in flight beat deeper rings).
 int cvt_stage_target_bytes() {
   static const int v = [] {
     const char* e = std::getenv("PMG_CVT_STAGE_KB");
-    int kb = e ? std::atoi(e) : 16;
+    int kb = e ? std::atoi(e) : 10;
     if (kb < 4) kb = 4;
     if (kb > kMaxStageBytes / 1024) kb = kMaxStageBytes / 1024;
     return kb * 1024;
@@ -2242,7 +2301,6 @@ int pmg_gather_tokens(const void* cache, int64_t cache_block_stride, int64_t cac
       pl.prm.R = num_reqs;
       pl.prm.t2s = token_to_seq;
       pl.prm.token_mode = 1;
-      pl.prm.spec = 0;
       return launch_one(pl, static_cast<cudaStream_t>(stream));
     }
   }

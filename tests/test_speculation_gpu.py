@@ -27,7 +27,8 @@ from gpu_helpers import assert_same
 pytestmark = pytest.mark.gpu
 
 R, STRIDE, B, NB = 3, 16, 16, 64
-META_INTS = 64  # cu at [0, R], block table at [16, 16 + R * STRIDE)
+T2S = 64         # token_to_seq at [T2S, T2S + 256)
+META_INTS = 320  # cu at [0, R], block table at [16, 16 + R * STRIDE)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -38,11 +39,15 @@ def _lib(cuda_lib):
 
 
 def _meta(rng, lens):
-    """A valid (cu, block table) pair packed into META_INTS int32."""
+    """Valid cu, block table and token_to_seq packed into META_INTS int32
+    (token_to_seq is -1 past the last request)."""
     m = np.zeros(META_INTS, np.int32)
     m[:R + 1] = np.concatenate([[0], np.cumsum(lens)])
     perm = rng.permutation(NB).astype(np.int32)
     m[16:16 + R * STRIDE] = perm[:R * STRIDE]
+    m[T2S:] = -1
+    for r in range(R):
+        m[T2S + m[r]:T2S + m[r + 1]] = r
     return m
 
 
@@ -93,5 +98,45 @@ def test_metadata_written_by_the_previous_grid(src, dst, same):
         assert np.array_equal(meta.cpu().numpy(), new)
         want, flag = _oracle(cache_bits, new, E, src, dst, wl.scale, T)
         got = out.cpu().view(torch.uint8).numpy().view(W.NP_BITS[W.ELEM_BYTES[dst]]).reshape(T, E)
+        assert int(err.item()) == flag == 0
+        assert_same(got, want, dst, src != dst)
+
+
+@pytest.mark.parametrize("src,dst", [("bf16", "bf16"), ("fp8_e4m3", "bf16")])
+def test_token_metadata_written_by_the_previous_grid(src, dst):
+    """The same race for the per-token entry point: token_to_seq, cu_seq_lens
+    and the block table come from the previous grid."""
+    dev = "cuda:0"
+    E = 64
+    rng = np.random.default_rng(74)
+    wl = W.make_workload("spec", [B * NB], None, B, E, NB, src, dst, 0.05, 75)
+    cache = wl.cache.to(dev)
+    cache_bits = W.tensor_bits(wl.cache)
+    scale = torch.tensor([wl.scale], dtype=torch.float32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    one_bt = torch.zeros(1, 1, dtype=torch.int32, device=dev)
+    one_cu = torch.tensor([0, 1], dtype=torch.int32, device=dev)
+    meta = torch.empty(META_INTS, dtype=torch.int32, device=dev)
+    for it in range(24):
+        new = _meta(rng, [int(x) for x in rng.integers(1, 5 * B, R)])
+        old = _meta(rng, [int(x) for x in rng.integers(1, 5 * B, R)])
+        T = int(new[R])
+        src_row = torch.from_numpy(new.view(np.float32).copy()).to(dev).view(1, 1, META_INTS)
+        meta.copy_(torch.from_numpy(old))
+        out = torch.full((T, E), 0, dtype=W.TORCH_DTYPES[dst], device=dev)
+        out.view(torch.uint8).fill_(0xA5)
+        err.zero_()
+        torch.cuda.synchronize()
+        torch.cuda._sleep(200_000)
+        binding.gather(src_row, meta.view(torch.float32).view(1, META_INTS), one_bt, one_cu, error_flag=err)
+        binding.gather_tokens(cache, out, meta[16:16 + R * STRIDE].view(R, STRIDE), meta[T2S:T2S + T],
+                              meta[:R + 1], scale, err, num_reqs=R)
+        torch.cuda.synchronize()
+        assert np.array_equal(meta.cpu().numpy(), new)
+        ed = W.ELEM_BYTES[dst]
+        want = np.full((T, E * ed), 0xA5, np.uint8).view(W.NP_BITS[ed])
+        flag = og.gather_tokens(cache_bits, new[16:16 + R * STRIDE].reshape(R, STRIDE).copy(),
+                                new[T2S:T2S + T].copy(), new[:R + 1].copy(), R, T, B, E, src, dst, wl.scale, want)
+        got = out.cpu().view(torch.uint8).numpy().view(W.NP_BITS[ed]).reshape(T, E)
         assert int(err.item()) == flag == 0
         assert_same(got, want, dst, src != dst)
