@@ -238,20 +238,16 @@ __device__ int build_plan(const Params& p, const PlanView& v, bool report_flags,
   int bad_start = 0;
   const uint64_t keep = evict_last_policy();
   for (int r = tid; r <= R; r += nt) {
-    int64_t c;
-    if (p.implied_end && r == R) {
-      const int64_t prev = R > 0 ? static_cast<int64_t>(ld_meta(p.cu + R - 1, keep)) : 0;
-      c = prev > T ? prev : T;
-    } else {
-      c = ld_meta(p.cu + r, keep);
-    }
+    // the three loads first, so that they share one round trip
+    const bool implied = p.implied_end && r == R;
+    const int64_t cur = implied ? 0 : static_cast<int64_t>(ld_meta(p.cu + r, keep));
+    const int64_t prev = r > 0 ? static_cast<int64_t>(ld_meta(p.cu + r - 1, keep)) : 0;
+    const int32_t start = (r < R && p.ss != nullptr) ? ld_meta(p.ss + r, keep) : 0;
+    const int64_t c = implied ? (prev > T ? prev : T) : cur;
     if (r == 0 && c < 0) bad = 1;
-    if (r > 0 && !(p.implied_end && r == R)) {
-      const int64_t prev = ld_meta(p.cu + r - 1, keep);
-      if (c < prev) bad = 1;
-    }
+    if (r > 0 && !implied && c < prev) bad = 1;
     v.ob[r] = static_cast<int32_t>(c < T ? c : T);
-    if (r < R) v.st[r] = p.ss ? ld_meta(p.ss + r, keep) : 0;
+    if (r < R) v.st[r] = start;
   }
   const bool any_bad = kWarp ? (__syncwarp(), __any_sync(0xffffffffu, bad)) : __syncthreads_or(bad);
   if (any_bad) {
