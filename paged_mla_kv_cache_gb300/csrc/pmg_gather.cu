@@ -226,7 +226,8 @@ __device__ __forceinline__ int32_t request_pages(const PlanView& v, int r, int B
 constexpr int kWarpPlanMaxReqs = 256;
 
 template <bool kWarp>
-__device__ int build_plan(const Params& p, const PlanView& v, bool report_flags, int* flags_out = nullptr) {
+__device__ int build_plan(const Params& p, const PlanView& v, bool report_flags, int* flags_out = nullptr,
+                          int32_t* raw_cu = nullptr) {
   __shared__ int32_t warp_sums[32];
   __shared__ int32_t total_pages;
   const int tid = kWarp ? static_cast<int>(threadIdx.x & 31) : static_cast<int>(threadIdx.x);
@@ -237,17 +238,41 @@ __device__ int build_plan(const Params& p, const PlanView& v, bool report_flags,
   int bad = 0;
   int bad_start = 0;
   const uint64_t keep = evict_last_policy();
-  for (int r = tid; r <= R; r += nt) {
-    // the three loads first, so that they share one round trip
-    const bool implied = p.implied_end && r == R;
-    const int64_t cur = implied ? 0 : static_cast<int64_t>(ld_meta(p.cu + r, keep));
-    const int64_t prev = r > 0 ? static_cast<int64_t>(ld_meta(p.cu + r - 1, keep)) : 0;
-    const int32_t start = (r < R && p.ss != nullptr) ? ld_meta(p.ss + r, keep) : 0;
-    const int64_t c = implied ? (prev > T ? prev : T) : cur;
-    if (r == 0 && c < 0) bad = 1;
-    if (r > 0 && !implied && c < prev) bad = 1;
-    v.ob[r] = static_cast<int32_t>(c < T ? c : T);
-    if (r < R) v.st[r] = start;
+  if constexpr (kWarp) {
+    // every CTA reads these few lines at once: one load per entry, and
+    // cu[r - 1] comes from the neighbouring lane (or the previous pass)
+    int64_t carry = 0;
+    for (int base = 0; base <= R; base += 32) {
+      const int r = base + tid;
+      const bool implied = p.implied_end && r == R;
+      const int32_t cur32 = (r <= R && !implied) ? ld_meta(p.cu + r, keep) : 0;
+      const int32_t start = (r < R && p.ss != nullptr) ? ld_meta(p.ss + r, keep) : 0;
+      if (raw_cu != nullptr && r <= R) raw_cu[r] = cur32;
+      const int64_t cur = cur32;
+      const int64_t up = __shfl_up_sync(0xffffffffu, cur, 1);
+      const int64_t prev = tid == 0 ? carry : up;
+      carry = __shfl_sync(0xffffffffu, cur, 31);
+      if (r <= R) {
+        const int64_t c = implied ? (prev > T ? prev : T) : cur;
+        if (r == 0 && c < 0) bad = 1;
+        if (r > 0 && !implied && c < prev) bad = 1;
+        v.ob[r] = static_cast<int32_t>(c < T ? c : T);
+        if (r < R) v.st[r] = start;
+      }
+    }
+  } else {
+    for (int r = tid; r <= R; r += nt) {
+      // the three loads first, so that they share one round trip
+      const bool implied = p.implied_end && r == R;
+      const int64_t cur = implied ? 0 : static_cast<int64_t>(ld_meta(p.cu + r, keep));
+      const int64_t prev = r > 0 ? static_cast<int64_t>(ld_meta(p.cu + r - 1, keep)) : 0;
+      const int32_t start = (r < R && p.ss != nullptr) ? ld_meta(p.ss + r, keep) : 0;
+      const int64_t c = implied ? (prev > T ? prev : T) : cur;
+      if (r == 0 && c < 0) bad = 1;
+      if (r > 0 && !implied && c < prev) bad = 1;
+      v.ob[r] = static_cast<int32_t>(c < T ? c : T);
+      if (r < R) v.st[r] = start;
+    }
   }
   const bool any_bad = kWarp ? (__syncwarp(), __any_sync(0xffffffffu, bad)) : __syncthreads_or(bad);
   if (any_bad) {
@@ -308,9 +333,10 @@ __device__ int build_plan(const Params& p, const PlanView& v, bool report_flags,
 
 // Before the previous grid is known to be done, a kernel may not read its
 // inputs, but it may warm L2 with them: a prefetch is not a read into
-// registers, and L2 is the point of coherence for later loads. Every CTA
-// prefetches the lines of cu_seq_lens and seq_starts; the CTAs of the launch
-// share the block table (tables up to 4 MB).
+// registers, and L2 is the point of coherence for later loads. The CTAs of
+// the launch share the lines out, one prefetch per line (every CTA reads the
+// same cu_seq_lens and seq_starts lines, and a line requested by hundreds of
+// CTAs at once is a hot spot), block tables up to 4 MB.
 __device__ __forceinline__ void prefetch_lines(const void* ptr, int64_t bytes, int64_t first_idx, int64_t step) {
   if (ptr == nullptr || bytes <= 0) return;
   const uintptr_t first = reinterpret_cast<uintptr_t>(ptr) & ~static_cast<uintptr_t>(127);
@@ -326,16 +352,21 @@ __device__ __forceinline__ void prefetch_metadata(const Params& p) {
     // token_to_seq spread over the grid; cu_seq_lens and the block table while small
     prefetch_lines(p.t2s, static_cast<int64_t>(p.T) * 4, static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x,
                    static_cast<int64_t>(gridDim.x) * blockDim.x);
-    if ((R + 1) * 4 <= (64ll << 10)) prefetch_lines(p.cu, (R + 1) * 4, threadIdx.x, blockDim.x);
+    if ((R + 1) * 4 <= (64ll << 10))
+      prefetch_lines(p.cu, (R + 1) * 4, static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x,
+                     static_cast<int64_t>(gridDim.x) * blockDim.x);
     const int64_t tb = R * p.bt_stride * 4;
     if (tb <= (4ll << 20))
       prefetch_lines(p.bt, tb, static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x,
                      static_cast<int64_t>(gridDim.x) * blockDim.x);
     return;
   }
+  // one prefetch per line across the grid: the lines are shared by every CTA
+  const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t gthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
   const int64_t cu_n = p.implied_end ? R : R + 1;
-  prefetch_lines(p.cu, cu_n * 4, threadIdx.x, blockDim.x);
-  prefetch_lines(p.ss, R * 4, threadIdx.x, blockDim.x);
+  prefetch_lines(p.cu, cu_n * 4, gtid, gthreads);
+  prefetch_lines(p.ss, R * 4, gtid, gthreads);
   const int64_t bt_bytes = R * p.bt_stride * 4;
   if (bt_bytes <= (4ll << 20))
     prefetch_lines(p.bt, bt_bytes, static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x,
@@ -756,6 +787,51 @@ __device__ __forceinline__ int spec_verdict(const SegQueue& q) {
   return v == 1 ? 1 : 0;
 }
 
+// The check of a speculative start (uses is 0): publishes the first batch
+// marked tentative when `publish`, waits for the previous grid, then reads
+// again every input the speculative plan sv read (cu_seq_lens as kept in
+// raw_cu, seq_starts) and, for a published batch, the block-table entry each
+// lane read, all in one round trip, and compares. Returns whether everything
+// still holds; for a published batch the verdict goes to the producer.
+__device__ __forceinline__ bool spec_confirm(const Params& p, const PlanView& sv, const int32_t* raw_cu, SegQueue& q,
+                                             const Segment& seg, int n, const SpecRead& rd, bool publish,
+                                             uint32_t& uses) {
+  const int lane = threadIdx.x & 31;
+  if (publish) {
+    q.seg[0][lane] = seg;
+    if (lane == 0) {
+      q.count[0] = n;
+      q.tentative = 1;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&q.full[0]);
+    uses = 1;
+  }
+  pdl_wait();
+  const uint64_t keep = evict_last_policy();
+  const int32_t phys_now = (publish && rd.idx >= 0) ? ld_meta(p.bt + rd.idx, keep) : 0;
+  bool same = !publish || rd.idx < 0 || phys_now == rd.phys;
+  for (int base = 0; base <= p.R; base += 128) {
+    int32_t c[4], st[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int r = base + 32 * j + lane;
+      const bool implied = p.implied_end && r == p.R;
+      c[j] = (r <= p.R && !implied) ? ld_meta(p.cu + r, keep) : 0;
+      st[j] = (r < p.R && p.ss != nullptr) ? ld_meta(p.ss + r, keep) : 0;
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int r = base + 32 * j + lane;
+      if (r <= p.R) same = same && c[j] == raw_cu[r];
+      if (r < p.R) same = same && st[j] == sv.st[r];
+    }
+  }
+  const bool valid = __all_sync(0xffffffffu, same);
+  if (publish && lane == 0) *reinterpret_cast<volatile int32_t*>(&q.verdict) = valid ? 1 : 2;
+  return valid;
+}
+
 // Publishes the 32 tokens t0 + lane (row source offset src, -1 for none) as
 // one batch: consecutive lanes whose source rows are one slot apart form one
 // segment. Returns the number of segments (0: nothing to publish) or -1 when
@@ -796,15 +872,19 @@ __device__ __forceinline__ int publish_tokens(const Params& p, SegQueue& q, uint
 // block-table read, bounds checks). Returns false on a timeout.
 //
 // Speculative start (p.spec, warp plans only): before the previous grid is
-// known to be done, the warp plans into the spare area sv and resolves the
-// first batch of its static item, reporting nothing, and publishes that batch
-// marked tentative, so that the producer can start its loads the moment the
-// wait returns (loads only read the cache, at addresses checked in bounds).
-// After the wait it reads the block-table entries again and plans again into
-// v from the inputs as they now are: if both plans and every entry agree, the
-// batch is what a plan after the wait would have produced and is confirmed;
-// otherwise it is withdrawn (its chunks are dropped unstored) and the item is
-// resolved again from the start.
+// known to be done, the warp plans into the spare area sv (keeping the raw
+// cu_seq_lens values it read) and resolves the first batch of its static item,
+// reporting nothing, and publishes that batch marked tentative, so that the
+// producer can start its loads the moment the wait returns (loads only read
+// the cache, at addresses checked in bounds). After the wait it reads every
+// input the plan and the batch used again, in one round trip, and compares:
+// if all agree, the plan and the batch are what they would have been after the
+// wait, the batch is confirmed and sv becomes the plan; otherwise the batch is
+// withdrawn (its chunks are dropped unstored) and the warp plans again into v
+// and resolves the item from the start. A kernel that starts after other work
+// runs its code cold in the instruction caches, so the check is a short loop
+// rather than a second run of the plan. The per-token mode does the same with
+// its first 32 tokens, checking every input they read.
 __device__ bool run_scheduler(const Params& p, const PlanView& v, const PlanView& sv, int32_t num_tasks,
                               SegQueue& q) {
   const int lane = threadIdx.x & 31;
@@ -812,6 +892,9 @@ __device__ bool run_scheduler(const Params& p, const PlanView& v, const PlanView
   uint32_t k = blockIdx.x;
   // first item only: -1 resolve from its first task, -2 already done, else resume at this task
   int32_t resume_t = -1;
+  PlanView pv = v;           // the plan in use
+  bool spec_first = false;   // pv is the speculative plan; its first batch is still to be checked
+  int32_t* raw_cu = nullptr;
   if (p.spec && p.token_mode) {
     // the first 32 tokens of the static item, checked after the wait by
     // reading every input they depended on again
@@ -835,62 +918,36 @@ __device__ bool run_scheduler(const Params& p, const PlanView& v, const PlanView
       if (valid) resume_t = r0 + 32u < r1 ? static_cast<int32_t>(r0 + 32u) : -2;
     }
   } else if (p.spec) {
+    raw_cu = sv.P + (p.R + 1);
     int plan_flags = 0;
-    const int32_t sn = build_plan<true>(p, sv, false, &plan_flags);
-    SpecRead rd{0, -1, 0};
-    Segment seg{};
-    int32_t t0 = 0;
-    int n = 0;
-    bool ok = false;
+    const int32_t sn = build_plan<true>(p, sv, false, &plan_flags, raw_cu);
     if (sn > 0 && plan_flags == 0) {
-      const Items si = make_items(sv, p);
-      uint32_t r0 = 0, r1 = 0;
-      if (k < si.n) item_rows(si, k, r0, r1);
-      if (r0 < r1) {
-        t0 = first_task_for_row(sv, p.R, p.B, r0);
-        const bool act = resolve_segment(p, sv, t0 + lane, sn, static_cast<int32_t>(r0), static_cast<int32_t>(r1),
-                                         seg, &rd);
-        n = __popc(__ballot_sync(0xffffffffu, act));
-        ok = n > 0 && __all_sync(0xffffffffu, rd.bits == 0);
-      }
-    }
-    if (ok) {
-      q.seg[0][lane] = seg;
-      if (lane == 0) {
-        q.count[0] = n;
-        q.tentative = 1;
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&q.full[0]);
-      uses = 1;
-    }
-    pdl_wait();
-    const int32_t phys_now = (ok && rd.idx >= 0) ? ld_meta(p.bt + rd.idx, evict_last_policy()) : 0;
-    num_tasks = build_plan<true>(p, v, blockIdx.x == 0);
-    if (ok) {
-      bool same = num_tasks == sn && phys_now == rd.phys;
-      const int words = 3 * p.R + 2;  // ob, st and P are contiguous
-      for (int i = lane; i < words; i += 32) same = same && v.ob[i] == sv.ob[i];
-      const bool valid = __all_sync(0xffffffffu, same);
-      if (lane == 0) *reinterpret_cast<volatile int32_t*>(&q.verdict) = valid ? 1 : 2;
-      if (valid) resume_t = n < kSegCap ? -2 : t0 + kSegCap;
+      // the main loop resolves the first batch from this plan and checks both
+      pv = sv;
+      num_tasks = sn;
+      spec_first = true;
+    } else {
+      pdl_wait();
+      num_tasks = build_plan<true>(p, v, blockIdx.x == 0);
     }
   }
   Items its{};
   bool have = false;
   if (num_tasks > 0) {
-    its = make_items(v, p);
+    its = make_items(pv, p);
     have = k < its.n;
   }
-  // with early metadata the workspace (claim counter) is touched only after
-  // the previous grid is done: wait after the first published batch
-  bool waited = p.early == 0;
+  // with early metadata or a speculative start the workspace (claim counter)
+  // is touched only after the previous grid is done: wait after the first
+  // published batch
+  bool waited = p.early == 0 && !spec_first;
   while (have) {
     // claim the next item now; its latency overlaps this item's resolution
     uint32_t claimed = 0;
     if (its.dynamic && lane == 0 && waited) claimed = gridDim.x + atomicAdd(reinterpret_cast<unsigned*>(p.sched), 1u);
     uint32_t r0, r1;
     item_rows(its, k, r0, r1);
+    bool replan = false;
     if (r0 < r1 && p.token_mode && resume_t != -2) {
       // 32 tokens per batch, one per lane, kTokGroup batches resolved together
       for (uint32_t g0 = resume_t >= 0 ? static_cast<uint32_t>(resume_t) : r0; g0 < r1; g0 += 32u * kTokGroup) {
@@ -904,12 +961,29 @@ __device__ bool run_scheduler(const Params& p, const PlanView& v, const PlanView
           if (publish_tokens(p, q, uses, g0 + 32u * j, srcs[j]) < 0) return false;
       }
     } else if (r0 < r1 && resume_t != -2) {
-      int32_t t = resume_t >= 0 ? resume_t : first_task_for_row(v, p.R, p.B, r0);
+      int32_t t = resume_t >= 0 ? resume_t : first_task_for_row(pv, p.R, p.B, r0);
       for (;;) {
         Segment seg;
-        const bool act = resolve_segment(p, v, t + lane, num_tasks, static_cast<int32_t>(r0),
-                                         static_cast<int32_t>(r1), seg);
+        SpecRead rd{0, -1, 0};
+        const bool act = resolve_segment(p, pv, t + lane, num_tasks, static_cast<int32_t>(r0),
+                                         static_cast<int32_t>(r1), seg, spec_first ? &rd : nullptr);
         const int n = __popc(__ballot_sync(0xffffffffu, act));
+        if (spec_first) {
+          // the first batch of a speculative start: published tentatively
+          // (unless it would report a flag), then checked after the wait
+          spec_first = false;
+          waited = true;
+          const bool publish = n > 0 && __all_sync(0xffffffffu, rd.bits == 0);
+          if (!spec_confirm(p, sv, raw_cu, q, seg, n, rd, publish, uses)) {
+            replan = true;
+            break;
+          }
+          if (its.dynamic && lane == 0) claimed = gridDim.x + atomicAdd(reinterpret_cast<unsigned*>(p.sched), 1u);
+          if (!publish) continue;  // the plan holds: resolve this batch again, reporting
+          if (n < kSegCap) break;
+          t += kSegCap;
+          continue;
+        }
         if (n == 0) break;
         const int b = static_cast<int>(uses % kSegBufs);
         if (uses >= kSegBufs && !mbar_wait_bounded(&q.empty[b], ((uses / kSegBufs) - 1u) & 1u)) return false;
@@ -923,6 +997,26 @@ __device__ bool run_scheduler(const Params& p, const PlanView& v, const PlanView
       }
     }
     resume_t = -1;
+    if (spec_first && !replan) {
+      // the static item gave no batch to check: check the plan alone
+      spec_first = false;
+      waited = true;
+      if (!spec_confirm(p, sv, raw_cu, q, Segment{}, 0, SpecRead{0, -1, 0}, false, uses)) replan = true;
+      else if (its.dynamic && lane == 0) claimed = gridDim.x + atomicAdd(reinterpret_cast<unsigned*>(p.sched), 1u);
+    }
+    if (replan) {
+      // the inputs changed under the speculative plan: plan again and start
+      // over from the static item (no claim was made yet)
+      num_tasks = build_plan<true>(p, v, blockIdx.x == 0);
+      pv = v;
+      k = blockIdx.x;
+      have = false;
+      if (num_tasks > 0) {
+        its = make_items(pv, p);
+        have = k < its.n;
+      }
+      continue;
+    }
     if (!waited) {
       pdl_wait();
       waited = true;
@@ -2100,7 +2194,10 @@ int launch_one(const Plan& pl, cudaStream_t stream) {
     KernelFn k = copy ? gather_bulk_kernel : tma_convert_kernel_for(pl.conv);
     if (k == nullptr) return PMG_ERR_UNSUPPORTED;
     const int threads = copy ? kBulkThreads : kCvtThreads;
-    const size_t plans = q.token_mode ? 0 : (q.spec ? 2 : 1) * host_plan_bytes(q.R);
+    // the speculative area also keeps the R + 1 entries of cu_seq_lens it read
+    const size_t plans = q.token_mode ? 0
+                         : q.spec ? 2 * host_plan_bytes(q.R) + (static_cast<size_t>(q.R) + 1) * sizeof(int32_t)
+                                  : host_plan_bytes(q.R);
     const size_t smem = static_cast<size_t>(q.stages) * q.stage_bytes + plans;
     int per_sm = 0;
     if (ctas_per_sm(k, threads, smem, &per_sm) != PMG_OK) return PMG_ERR_CUDA;
