@@ -48,6 +48,7 @@ PROFILE_FILES = {
     "60k": "gather_bulk_single60k.md",
     "300k": "gather_bulk_single300k.md",
     "skew8": "gather_tma_convert_skew8.md",
+    "skew64_raw": "gather_bulk_skew64_raw.md",
     "skew64_dequant": "gather_tma_convert_skew64_dequant.md",
 }
 KERNEL_SRC = os.path.join(ROOT, "paged_mla_kv_cache_gb300", "csrc", "pmg_gather.cu")

@@ -738,17 +738,28 @@ __device__ __forceinline__ void resolve_tokens(const Params& p, uint32_t t_first
   }
 }
 
-// Whether the token's inputs still hold what `r` recorded (token t < t_end).
-// The loads go to the recorded addresses and are issued together.
-__device__ __forceinline__ bool token_unchanged(const Params& p, uint32_t t, uint32_t t_end, const TokRead& r) {
-  if (t >= t_end) return true;
+// Whether the inputs of tokens t_first + 32 j (j < N, below t_end) still hold
+// what rec recorded. The loads go to the recorded addresses and are all
+// issued before any comparison.
+template <int N>
+__device__ __forceinline__ bool tokens_unchanged(const Params& p, uint32_t t_first, uint32_t t_end,
+                                                 const TokRead (&rec)[N]) {
   const uint64_t keep = evict_last_policy();
-  const bool in = r.b >= 0 && r.b < p.R;
-  const int32_t b = ld_meta(p.t2s + t, keep);
-  const int32_t c0 = in ? ld_meta(p.cu + r.b, keep) : 0;
-  const int32_t c1 = in ? ld_meta(p.cu + r.b + 1, keep) : 0;
-  const int32_t ph = r.idx >= 0 ? ld_meta(p.bt + r.idx, keep) : 0;
-  return b == r.b && c0 == r.c0 && c1 == r.c1 && ph == (r.idx >= 0 ? r.phys : 0);
+  int32_t b[N], c0[N], c1[N], ph[N];
+#pragma unroll
+  for (int j = 0; j < N; ++j) {
+    const uint32_t t = t_first + 32u * j;
+    const bool in = rec[j].b >= 0 && rec[j].b < p.R;
+    b[j] = t < t_end ? ld_meta(p.t2s + t, keep) : rec[j].b;
+    c0[j] = (t < t_end && in) ? ld_meta(p.cu + rec[j].b, keep) : rec[j].c0;
+    c1[j] = (t < t_end && in) ? ld_meta(p.cu + rec[j].b + 1, keep) : rec[j].c1;
+    ph[j] = (t < t_end && rec[j].idx >= 0) ? ld_meta(p.bt + rec[j].idx, keep) : rec[j].phys;
+  }
+  bool same = true;
+#pragma unroll
+  for (int j = 0; j < N; ++j)
+    same = same && b[j] == rec[j].b && c0[j] == rec[j].c0 && c1[j] == rec[j].c1 && ph[j] == rec[j].phys;
+  return same;
 }
 
 // Segment batches handed from the scheduler warp to the producer thread.
@@ -890,33 +901,12 @@ __device__ bool run_scheduler(const Params& p, const PlanView& v, const PlanView
   const int lane = threadIdx.x & 31;
   uint32_t uses = 0;
   uint32_t k = blockIdx.x;
-  // first item only: -1 resolve from its first task, -2 already done, else resume at this task
-  int32_t resume_t = -1;
   PlanView pv = v;           // the plan in use
   bool spec_first = false;   // pv is the speculative plan; its first batch is still to be checked
   int32_t* raw_cu = nullptr;
+  bool tok_spec = false;     // token mode: the first group of the static item is to be checked
   if (p.spec && p.token_mode) {
-    // the first 32 tokens of the static item, checked after the wait by
-    // reading every input they depended on again
-    const Items si = make_items(v, p);
-    uint32_t r0 = 0, r1 = 0;
-    if (k < si.n) item_rows(si, k, r0, r1);
-    int64_t src[1] = {-1};
-    TokRead rec[1] = {TokRead{0, 0, 0, 0, -1}};
-    int bits = 0;
-    if (r0 < r1) resolve_tokens<1>(p, r0 + static_cast<uint32_t>(lane), r1, src, bits, rec);
-    const bool ok = r0 < r1 && __all_sync(0xffffffffu, bits == 0) && __any_sync(0xffffffffu, src[0] >= 0);
-    if (ok) {
-      if (lane == 0) q.tentative = 1;
-      (void)publish_tokens(p, q, uses, r0, src[0]);  // the first batch: no wait
-    }
-    pdl_wait();
-    if (ok) {
-      const bool same = token_unchanged(p, r0 + static_cast<uint32_t>(lane), r1, rec[0]);
-      const bool valid = __all_sync(0xffffffffu, same);
-      if (lane == 0) *reinterpret_cast<volatile int32_t*>(&q.verdict) = valid ? 1 : 2;
-      if (valid) resume_t = r0 + 32u < r1 ? static_cast<int32_t>(r0 + 32u) : -2;
-    }
+    tok_spec = true;
   } else if (p.spec) {
     raw_cu = sv.P + (p.R + 1);
     int plan_flags = 0;
@@ -940,7 +930,7 @@ __device__ bool run_scheduler(const Params& p, const PlanView& v, const PlanView
   // with early metadata or a speculative start the workspace (claim counter)
   // is touched only after the previous grid is done: wait after the first
   // published batch
-  bool waited = p.early == 0 && !spec_first;
+  bool waited = p.early == 0 && !spec_first && !tok_spec;
   while (have) {
     // claim the next item now; its latency overlaps this item's resolution
     uint32_t claimed = 0;
@@ -948,20 +938,44 @@ __device__ bool run_scheduler(const Params& p, const PlanView& v, const PlanView
     uint32_t r0, r1;
     item_rows(its, k, r0, r1);
     bool replan = false;
-    if (r0 < r1 && p.token_mode && resume_t != -2) {
+    if (r0 < r1 && p.token_mode) {
       // 32 tokens per batch, one per lane, kTokGroup batches resolved together
-      for (uint32_t g0 = resume_t >= 0 ? static_cast<uint32_t>(resume_t) : r0; g0 < r1; g0 += 32u * kTokGroup) {
+      for (uint32_t g0 = r0; g0 < r1; g0 += 32u * kTokGroup) {
         int64_t srcs[kTokGroup];
         TokRead rec[kTokGroup];
         int bits = 0;
         resolve_tokens<kTokGroup>(p, g0 + static_cast<uint32_t>(lane), r1, srcs, bits, rec);
+        int first = 0;  // batches of this group already published
+        if (tok_spec) {
+          // speculative start: the group's first batch goes out tentatively
+          // (unless the group would report a flag); after the wait every input
+          // the group read is read again in one round trip and compared
+          tok_spec = false;
+          waited = true;
+          const bool publish = __all_sync(0xffffffffu, bits == 0) && __any_sync(0xffffffffu, srcs[0] >= 0);
+          if (publish) {
+            if (lane == 0) q.tentative = 1;
+            (void)publish_tokens(p, q, uses, g0, srcs[0]);  // the first batch: no wait
+          }
+          pdl_wait();
+          const bool valid = __all_sync(0xffffffffu, tokens_unchanged<kTokGroup>(p, g0 + static_cast<uint32_t>(lane),
+                                                                                   r1, rec));
+          if (publish && lane == 0) *reinterpret_cast<volatile int32_t*>(&q.verdict) = valid ? 1 : 2;
+          if (its.dynamic && lane == 0) claimed = gridDim.x + atomicAdd(reinterpret_cast<unsigned*>(p.sched), 1u);
+          if (!valid) {
+            // inputs changed: resolve the group again (the tentative batch is withdrawn)
+            g0 -= 32u * kTokGroup;
+            continue;
+          }
+          if (publish) first = 1;
+        }
         if (bits != 0) set_flag(p, bits);
 #pragma unroll
         for (int j = 0; j < kTokGroup; ++j)
-          if (publish_tokens(p, q, uses, g0 + 32u * j, srcs[j]) < 0) return false;
+          if (j >= first && publish_tokens(p, q, uses, g0 + 32u * j, srcs[j]) < 0) return false;
       }
-    } else if (r0 < r1 && resume_t != -2) {
-      int32_t t = resume_t >= 0 ? resume_t : first_task_for_row(pv, p.R, p.B, r0);
+    } else if (r0 < r1 && !p.token_mode) {
+      int32_t t = first_task_for_row(pv, p.R, p.B, r0);
       for (;;) {
         Segment seg;
         SpecRead rd{0, -1, 0};
@@ -996,7 +1010,7 @@ __device__ bool run_scheduler(const Params& p, const PlanView& v, const PlanView
         t += kSegCap;
       }
     }
-    resume_t = -1;
+    tok_spec = false;  // an empty static item leaves nothing to check
     if (spec_first && !replan) {
       // the static item gave no batch to check: check the plan alone
       spec_first = false;
