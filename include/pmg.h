@@ -21,6 +21,14 @@
  *    dimension has stride 1.
  *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *    stream). Calls are asynchronous on that stream and never synchronise.
+ *  - Kernels are launched with programmatic dependent launch. With up to 256
+ *    requests (and for pmg_gather_tokens) the TMA paths read cu_seq_lens,
+ *    seq_starts, token_to_seq and block_table once before the previous kernel
+ *    in the stream has finished, plan from those values, and read every value
+ *    they used again after it has finished; they use the early plan only if
+ *    nothing changed. The result is always that of the inputs as they are
+ *    when the previous kernel has finished. Nothing is written, and no cache,
+ *    scale or workspace byte is read into a result, before that point.
  *  - Host-detected errors return a non-zero pmg_status synchronously; nothing
  *    is launched and no output is touched.
  *  - Data errors found on the device (values inside cu_seq_lens, seq_starts or
