@@ -627,7 +627,12 @@ struct Items {
 // moment the launch may read the cache, while a claimed item waits for its
 // claim, so a CTA with little work needs a static head start covering that
 // latency (skew-8: 60 rows per CTA, 0.77 -> 0.81 of peak). Dynamic items are
-// about rows / (16 G) rows and never smaller than one ring stage.
+// about rows / (64 G) rows and never smaller than one ring stage: small items
+// even out the CTAs' finishing times (single-300K 0.975 -> 0.988), but an item
+// must carry more data than the claim and block-table round trips that fetch
+// it (half-stage items lost 10% on single-60K). Token mode resolves an item
+// through three dependent round trips instead of one and keeps items four
+// times larger (rows / (16 G)).
 __device__ __forceinline__ Items make_items(const PlanView& v, const Params& p) {
   Items it;
   it.lo = p.token_mode ? 0u : static_cast<uint32_t>(v.ob[0]);
@@ -640,7 +645,7 @@ __device__ __forceinline__ Items make_items(const PlanView& v, const Params& p) 
     const uint32_t rps = static_cast<uint32_t>(p.rows_per_stage > 0 ? p.rows_per_stage : 1);
     const uint32_t head = 2u * rps < rows / G ? 2u * rps : rows / G;
     if (it.a < head) it.a = head;
-    const uint32_t d = rows / (16u * G);
+    const uint32_t d = rows / ((p.token_mode ? 16u : 64u) * G);
     const uint32_t dmin = static_cast<uint32_t>(p.rows_per_stage > 0 ? p.rows_per_stage : 1);
     it.d = d > dmin ? d : dmin;
     const uint32_t rest = rows - G * it.a;
