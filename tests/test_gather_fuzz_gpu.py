@@ -59,3 +59,31 @@ def test_random_gather(seed):
     assert guards, "guard regions written"
     assert flag == oflag
     assert_same(got, want, wl.dst_dtype, wl.src_dtype != wl.dst_dtype)
+
+
+def _case_many(seed):
+    """100 to 300 requests: several passes of the plan and its check, and both
+    sides of the 256-request limit of the one-warp plan."""
+    rng = np.random.default_rng(95_000 + seed)
+    src, dst = PAIRS[int(rng.integers(0, len(PAIRS)))]
+    B = int(rng.choice([1, 16, 64]))
+    E = int(rng.choice([8, 64, 576]))
+    R = int(rng.integers(100, 301))
+    lens = [int(x) if rng.random() > 0.15 else 0 for x in rng.integers(0, 2 * B + 9, R)]
+    starts = [int(x) for x in rng.integers(0, B + 1, R)] if rng.random() < 0.6 else None
+    total = sum(lens) - int(rng.integers(0, 10))
+    wl = W.make_workload("fuzz-many", lens, starts, B, E, None, src, dst, 0.05, 95_000 + seed,
+                         total_tokens=max(total, 0))
+    return wl, int(rng.choice(OPTIONS)), bool(rng.random() < 0.5)
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_random_gather_many_requests(seed):
+    wl, options, workspace = _case_many(seed)
+    case = DeviceCase(wl, workspace=workspace)
+    case.run(options=options)
+    got, flag, guards = case.result()
+    want, oflag = oracle_run(wl)
+    assert guards, "guard regions written"
+    assert flag == oflag
+    assert_same(got, want, wl.dst_dtype, wl.src_dtype != wl.dst_dtype)

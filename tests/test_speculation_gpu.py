@@ -140,3 +140,63 @@ def test_token_metadata_written_by_the_previous_grid(src, dst):
         got = out.cpu().view(torch.uint8).numpy().view(W.NP_BITS[ed]).reshape(T, E)
         assert int(err.item()) == flag == 0
         assert_same(got, want, dst, src != dst)
+
+
+def _align4(n):
+    return (n + 3) // 4 * 4
+
+
+@pytest.mark.parametrize("R,with_ss,implied", [(200, True, False), (130, False, True), (40, True, True),
+                                               (256, True, False)])
+def test_many_requests_metadata_race(R, with_ss, implied):
+    """The same race with a larger batch: the check after the wait reads
+    cu_seq_lens and seq_starts in several passes of 128 entries; seq_starts
+    and the implied-end convention change under the race too."""
+    dev = "cuda:0"
+    B, E, NB2, STRIDE2 = 16, 64, 1024, 4
+    rng = np.random.default_rng(700 + R + 7 * with_ss + 3 * implied)
+    wl = W.make_workload("spec", [B * NB2], None, B, E, NB2, "bf16", "bf16", 1.0, 76)
+    cache = wl.cache.to(dev)
+    cache_bits = W.tensor_bits(wl.cache)
+    SS = _align4(R + 1)
+    BT = SS + _align4(R)
+    META = _align4(BT + R * STRIDE2)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    one_bt = torch.zeros(1, 1, dtype=torch.int32, device=dev)
+    one_cu = torch.tensor([0, 1], dtype=torch.int32, device=dev)
+    meta = torch.empty(META, dtype=torch.int32, device=dev)
+    opts = binding.OPT_IMPLIED_END if implied else 0
+
+    def make():
+        lens = rng.integers(0, 2 * B + 1, R)
+        starts = rng.integers(0, B, R) if with_ss else np.zeros(R, np.int64)
+        m = np.zeros(META, np.int32)
+        m[:R + 1] = np.concatenate([[0], np.cumsum(lens)])
+        m[SS:SS + R] = starts
+        m[BT:BT + R * STRIDE2] = rng.permutation(NB2)[:R * STRIDE2]
+        return m
+
+    for it in range(12):
+        new, old = make(), make()
+        T = int(new[R])
+        src_row = torch.from_numpy(new.view(np.float32).copy()).to(dev).view(1, 1, META)
+        meta.copy_(torch.from_numpy(old))
+        out = torch.empty((T, E), dtype=torch.bfloat16, device=dev)
+        out.view(torch.uint8).fill_(0xA5)
+        err.zero_()
+        torch.cuda.synchronize()
+        torch.cuda._sleep(200_000)
+        binding.gather(src_row, meta.view(torch.float32).view(1, META), one_bt, one_cu, error_flag=err)
+        binding.gather(cache, out, meta[BT:BT + R * STRIDE2].view(R, STRIDE2), meta[:R + (0 if implied else 1)],
+                       meta[SS:SS + R] if with_ss else None, None, err, num_reqs=R, options=opts)
+        torch.cuda.synchronize()
+        assert np.array_equal(meta.cpu().numpy(), new)
+        cu = new[:R + 1].copy()
+        if implied:
+            cu[R] = max(T, int(cu[R - 1]))
+        want = np.full((T, E), 0xA5A5, np.uint16)
+        flag = og.gather(cache_bits, new[BT:BT + R * STRIDE2].reshape(R, STRIDE2).copy(), cu,
+                         new[SS:SS + R].copy() if with_ss else None, R, T, B, E, "bf16", "bf16", 1.0, want)
+        got = out.cpu().view(torch.int16).numpy().view(np.uint16)
+        assert int(err.item()) == flag == 0
+        assert_same(got, want, "bf16", False)
