@@ -16,9 +16,10 @@
 //    grid (a multiple of the SM count) splits the OUTPUT ROWS across CTAs, so a
 //    300K-token request and a 17-token request cost each CTA the same bytes;
 //    inside its rows a CTA walks page tasks in order. With a caller workspace,
-//    a quarter of the rows is split up front and the rest is claimed in
-//    stage-sized items through an atomic counter, which evens out CTAs whose
-//    memory traffic is served at different speeds.
+//    each CTA takes a static head (a quarter of its rows, at least two ring
+//    stages) and the rest is claimed in stage-sized items through an atomic
+//    counter, which evens out CTAs whose memory traffic is served at
+//    different speeds.
 //  * Page-task mapper. The exclusive prefix sum of per-request page counts is
 //    built in shared memory (by one warp for up to 256 requests, by the CTA
 //    up to 4096; larger batches run as groups). A flat task id becomes (req,
@@ -33,10 +34,15 @@
 //    bulk stores) driven by one thread. Converting gathers bulk-load source
 //    rows into a ring that converter warps turn into 16-byte stores. Rows that
 //    are not 16-byte aligned take SIMT loads and stores of 16, 8, 4, 2 or 1
-//    bytes. A per-token variant maps each output row through token_to_seq.
+//    bytes. The per-token entry point maps each output row through
+//    token_to_seq; on the TMA kernels that is a mode of the scheduler warp,
+//    which merges runs of adjacent source rows into bulk segments.
 //  * Launch. Programmatic dependent launch: metadata is prefetched into L2
-//    while the previous grid finishes; inputs are read only after it completes
-//    (or, with the caller's early-metadata promise, the plan runs before).
+//    while the previous grid finishes. The TMA kernels plan and resolve their
+//    first batch from it before that grid completes and confirm both by
+//    reading every input used again afterwards (or skip the check under the
+//    caller's early-metadata promise); the cache is read and dst written only
+//    after it completes.
 //  * Safety. 64-bit byte offsets everywhere; the logical block is checked
 //    against block_table_stride and the physical id against num_blocks in
 //    every path (the review section "评论区精华" reports both checks missing
