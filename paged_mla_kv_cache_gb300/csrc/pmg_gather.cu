@@ -816,6 +816,32 @@ __device__ __forceinline__ int spec_verdict(const SegQueue& q) {
   return v == 1 ? 1 : 0;
 }
 
+// Warms L2 (and the address translation) with the source rows of a batch
+// published before the wait, at most cap rows in segment order, the lines
+// spread over the warp's lanes. A prefetch reads nothing into registers: if
+// the previous grid still writes those rows, the loads after the wait read
+// them as they are then, and rows of a withdrawn batch are only wasted
+// bandwidth. Every address is inside a row the batch's checks accepted.
+__device__ __forceinline__ void prefetch_batch(const Params& p, const SegQueue& q, int b, int32_t cap) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t rb = static_cast<uint32_t>(p.row_src_bytes);
+  const uint32_t lpr = (rb + 127u) / 128u;  // lines a row touches from its start
+  const int n = q.count[b];
+  for (int i = 0; i < n && cap > 0; ++i) {
+    const Segment sg = q.seg[b][i];
+    const int32_t rows = sg.nrows < cap ? sg.nrows : cap;
+    cap -= rows;
+    const uint32_t units = static_cast<uint32_t>(rows) * lpr;
+    for (uint32_t u = static_cast<uint32_t>(lane); u < units; u += 32u) {
+      const uint32_t row = u / lpr;
+      const uint32_t line = u - row * lpr;
+      const uint32_t off = line * 128u < rb ? line * 128u : rb - 1u;
+      const uint8_t* a = p.cache + sg.src + static_cast<int64_t>(row) * p.tok_stride_b + off;
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+    }
+  }
+}
+
 // The check of a speculative start (uses is 0): publishes the first batch
 // marked tentative when `publish`, waits for the previous grid, then reads
 // again every input the speculative plan sv read (cu_seq_lens as kept in
@@ -835,6 +861,7 @@ __device__ __forceinline__ bool spec_confirm(const Params& p, const PlanView& sv
     __syncwarp();
     if (lane == 0) mbar_arrive(&q.full[0]);
     uses = 1;
+    prefetch_batch(p, q, 0, 2 * p.rows_per_stage);
   }
   pdl_wait();
   const uint64_t keep = evict_last_policy();
@@ -974,6 +1001,8 @@ __device__ bool run_scheduler(const Params& p, const PlanView& v, const PlanView
           if (publish) {
             if (lane == 0) q.tentative = 1;
             (void)publish_tokens(p, q, uses, g0, srcs[0]);  // the first batch: no wait
+            __syncwarp();
+            prefetch_batch(p, q, 0, 2 * p.rows_per_stage);
           }
           pdl_wait();
           const bool valid = __all_sync(0xffffffffu, tokens_unchanged<kTokGroup>(p, g0 + static_cast<uint32_t>(lane),
@@ -1024,6 +1053,7 @@ __device__ bool run_scheduler(const Params& p, const PlanView& v, const PlanView
         __syncwarp();
         if (lane == 0) mbar_arrive(&q.full[b]);
         ++uses;
+        if (!waited && uses == 1) prefetch_batch(p, q, b, 2 * p.rows_per_stage);  // early metadata
         if (n < kSegCap) break;
         t += kSegCap;
       }
