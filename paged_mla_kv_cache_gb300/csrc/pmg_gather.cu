@@ -105,6 +105,7 @@ struct Params {
   const int32_t* gate;    // large batches: non-zero when cu_seq_lens failed validation (write nothing)
   int32_t early;          // plan and first block ids before the previous grid completes (caller's promise)
   int32_t spec;           // plan and first batch before the previous grid completes, checked after it
+  int32_t prefetch_rows;  // rows of the pre-wait batch warmed in L2
   const int32_t* t2s;     // per-token gather: request of each output row (token mode)
   int32_t token_mode;     // 1: rows [0, T) map through t2s instead of the page plan
   int32_t sched_static_pct;  // dynamic mode: share of rows split statically up front
@@ -861,7 +862,7 @@ __device__ __forceinline__ bool spec_confirm(const Params& p, const PlanView& sv
     __syncwarp();
     if (lane == 0) mbar_arrive(&q.full[0]);
     uses = 1;
-    prefetch_batch(p, q, 0, 2 * p.rows_per_stage);
+    prefetch_batch(p, q, 0, p.prefetch_rows);
   }
   pdl_wait();
   const uint64_t keep = evict_last_policy();
@@ -1002,7 +1003,7 @@ __device__ bool run_scheduler(const Params& p, const PlanView& v, const PlanView
             if (lane == 0) q.tentative = 1;
             (void)publish_tokens(p, q, uses, g0, srcs[0]);  // the first batch: no wait
             __syncwarp();
-            prefetch_batch(p, q, 0, 2 * p.rows_per_stage);
+            prefetch_batch(p, q, 0, p.prefetch_rows);
           }
           pdl_wait();
           const bool valid = __all_sync(0xffffffffu, tokens_unchanged<kTokGroup>(p, g0 + static_cast<uint32_t>(lane),
@@ -1053,7 +1054,7 @@ __device__ bool run_scheduler(const Params& p, const PlanView& v, const PlanView
         __syncwarp();
         if (lane == 0) mbar_arrive(&q.full[b]);
         ++uses;
-        if (!waited && uses == 1) prefetch_batch(p, q, b, 2 * p.rows_per_stage);  // early metadata
+        if (!waited && uses == 1) prefetch_batch(p, q, b, p.prefetch_rows);  // early metadata
         if (n < kSegCap) break;
         t += kSegCap;
       }
@@ -1896,6 +1897,15 @@ int sched_static_pct() {
   static const int v = env_int("PMG_SCHED_STATIC_PCT", 25, 0, 100);
   return v;
 }
+// Ring stages' worth of rows of the pre-wait batch prefetched into L2
+// (PMG_PREFETCH_STAGES, 0..8). A full ring (4) measured best: single-300K
+// 0.987 -> 1.002 of the copy peak, skew-64 dequant 0.902 -> 0.924; 8 loses
+// on the padded raw rows.
+int prefetch_stages() {
+  static const int v = env_int("PMG_PREFETCH_STAGES", 4, 0, kMaxStages);
+  return v;
+}
+
 // Speculative start of the TMA paths (PMG_SPEC=0 turns it off).
 bool use_spec() {
   static const int v = env_int("PMG_SPEC", 1, 0, 1);
@@ -2054,6 +2064,7 @@ int make_plan(const void* cache, int64_t cbs, int64_t cts, int64_t num_blocks, c
     q.rows_per_stage = rows;
     q.stage_bytes = rows * q.row_src_bytes;
     q.stages = bulk_stages();
+    q.prefetch_rows = prefetch_stages() * rows;
     out.unit = 0;
   } else {
     int64_t upr;
@@ -2065,6 +2076,7 @@ int make_plan(const void* cache, int64_t cbs, int64_t cts, int64_t num_blocks, c
       q.rows_per_stage = rows;
       q.stage_bytes = rows * q.row_src_bytes;
       q.stages = cvt_stages();
+      q.prefetch_rows = prefetch_stages() * rows;
       q.dense = q.dst_dense;
     } else {
       const int64_t unit_elems = (conv == CONV_COPY) ? unit / es : unit;
