@@ -1019,8 +1019,19 @@ __device__ bool run_scheduler(const Params& p, const PlanView& v, const PlanView
         }
         if (bits != 0) set_flag(p, bits);
 #pragma unroll
-        for (int j = 0; j < kTokGroup; ++j)
-          if (j >= first && publish_tokens(p, q, uses, g0 + 32u * j, srcs[j]) < 0) return false;
+        for (int j = 0; j < kTokGroup; ++j) {
+          if (j < first) continue;
+          if (uses >= kSegBufs && !waited) {
+            // Before the wait only the free batches may be filled: waiting
+            // for the producer to free one would mean waiting for the
+            // previous grid through a bounded wait. The wait (and this
+            // item's claim) comes first.
+            pdl_wait();
+            waited = true;
+            if (its.dynamic && lane == 0) claimed = gridDim.x + atomicAdd(reinterpret_cast<unsigned*>(p.sched), 1u);
+          }
+          if (publish_tokens(p, q, uses, g0 + 32u * j, srcs[j]) < 0) return false;
+        }
       }
     } else if (r0 < r1 && !p.token_mode) {
       int32_t t = first_task_for_row(pv, p.R, p.B, r0);
@@ -1047,6 +1058,12 @@ __device__ bool run_scheduler(const Params& p, const PlanView& v, const PlanView
           continue;
         }
         if (n == 0) break;
+        if (uses >= kSegBufs && !waited) {
+          // as in token mode: no wait on the producer before the wait
+          pdl_wait();
+          waited = true;
+          if (its.dynamic && lane == 0) claimed = gridDim.x + atomicAdd(reinterpret_cast<unsigned*>(p.sched), 1u);
+        }
         const int b = static_cast<int>(uses % kSegBufs);
         if (uses >= kSegBufs && !mbar_wait_bounded(&q.empty[b], ((uses / kSegBufs) - 1u) & 1u)) return false;
         q.seg[b][lane] = seg;
