@@ -5,22 +5,37 @@ call / device time, and its fraction of the measured HBM copy peak. A step is
 one gather call (the whole hot path: plan, page mapping, block-table lookups,
 data movement) over one batch of synthetic input.
 
-Default workload: single-60K raw gather (1 request of 60,000 tokens, block
-size 64, 576-element bf16 entries, 1024 shuffled blocks). Inputs are resident
-in HBM. Consecutive steps rotate over several identical replicas of the inputs
-whose combined footprint is more than four times the L2 cache, so no step
-finds its data in L2 (no flush inside the timed region). A second, separate
-measurement ("cold") flushes L2 by writing a 512 MB buffer before every call
-and reports the median call time, the way the page measured its kernels.
+Headline workload: single-300K raw gather (1 request of 300,000 tokens, block
+size 64, 576-element bf16 entries, 5000 shuffled blocks), the largest of the
+named single-GPU workloads. Inputs are resident in HBM. Consecutive steps
+rotate over identical replicas of the inputs whose combined footprint is more
+than four times the L2 cache, so no step finds its data in L2 (no flush inside
+the timed region). The K timed steps are replayed from CUDA graphs; the region
+of exactly K steps is timed several times (so that the clock sampler sees the
+GPU under load even for small K) and the median region gives the line's value.
+
+Beside the headline the line carries:
+  per_config  every named target workload (single-60K, single-300K, skew-8,
+              skew-64 raw and dequant, and a 1M-token fp32 copy whose output
+              offsets pass 2^31 bytes): steady-state GB/s and fraction of
+              peak, per-launch time, and two "cold" medians with L2 flushed
+              before every call, the page's cold-cache way of timing its
+              kernels: "cold" writes a 512 MB buffer, "cold_clean" also reads
+              it back (so L2 holds clean lines of another buffer).
+  e2e         the same metric through the public binding with pinned host
+              buffers, host<->device copies inside the timed region.
+  cpu_baseline  the CPU oracle on the host cores (single thread, and all cores
+              as concurrent oracle calls over disjoint row ranges).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                       [--config 60k|tiny|300k|skew8|skew64_raw|skew64_dequant]
+                       [--config 300k|60k|tiny|skew8|skew64_raw|skew64_dequant|fp32_1m]
 Under torchrun (N > 1) every rank runs its own replica of the workload (weak
 scaling, no collective on the data path); rank 0 prints one JSON line.
 """
 from __future__ import annotations
 
 import argparse
+import concurrent.futures
 import hashlib
 import json
 import math
@@ -43,7 +58,10 @@ from paged_mla_kv_cache_gb300 import workloads as W  # noqa: E402
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
 METRIC = "effective gather GB/s (read+write / device time) and % of GB300 HBM peak"
-# committed ncu summary of the dominant kernel per workload
+HEADLINE = "300k"
+PER_CONFIG = ["60k", "300k", "skew8", "skew64_raw", "skew64_dequant", "fp32_1m"]
+# Committed ncu captures of the dominant kernel per workload: DRAM bytes over
+# several consecutive launches of the timed step, divided by the launch count.
 PROFILE_FILES = {
     "60k": "gather_bulk_single60k.md",
     "300k": "gather_bulk_single300k.md",
@@ -52,6 +70,10 @@ PROFILE_FILES = {
     "skew64_dequant": "gather_tma_convert_skew64_dequant.md",
 }
 KERNEL_SRC = os.path.join(ROOT, "paged_mla_kv_cache_gb300", "csrc", "pmg_gather.cu")
+# how L2 is kept out of the steady-state figure; one statement for both arms
+L2_POLICY = ("each GPU step reads and writes inputs/outputs not touched by the previous steps "
+             "(rotating replicas, >= 4x L2 in all), no flush in the timed region; the cold figures flush "
+             "L2 before every call")
 
 
 def dist_env():
@@ -97,8 +119,10 @@ def kernel_code_hash(text: str) -> str:
 
 
 def profiled_traffic(config: str):
-    """DRAM bytes per launch from the committed ncu summary of this workload, if
-    it was taken on the current kernel code (else None)."""
+    """DRAM read and write bytes per launch from the committed ncu capture of
+    this workload (consecutive launches of the timed step), if it was taken on
+    the current kernel code; else None. This is a stored capture, not a
+    measurement of this run: the line labels it so."""
     name = PROFILE_FILES.get(config)
     if name is None:
         return None
@@ -107,11 +131,39 @@ def profiled_traffic(config: str):
     except OSError:
         return None
     m_sha = re.search(r"kernel_code_sha256:\s*([0-9a-f]{64})", text)
-    m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
-    if not (m_sha and m_tr):
+    m_rd = re.search(r"dram_read_bytes_per_launch:\s*([0-9]+)", text)
+    m_wr = re.search(r"dram_write_bytes_per_launch:\s*([0-9]+)", text)
+    m_n = re.search(r"launches_captured:\s*([0-9]+)", text)
+    if not (m_sha and m_rd and m_wr):
         return None
-    sha = kernel_code_hash(open(KERNEL_SRC).read())
-    return int(m_tr.group(1)) if sha == m_sha.group(1) else None
+    if kernel_code_hash(open(KERNEL_SRC).read()) != m_sha.group(1):
+        return None
+    return {"read": int(m_rd.group(1)), "write": int(m_wr.group(1)),
+            "source": f"committed ncu capture profiles/{name}: dram__bytes_read.sum and dram__bytes_write.sum "
+                      f"over {m_n.group(1) if m_n else 'several'} consecutive launches of the timed step, "
+                      f"per launch (same kernel code hash)"}
+
+
+def cpu_facts():
+    """Host core count and CPU model of the machine the oracle runs on."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    if model is None:
+        try:
+            for line in open("/proc/cpuinfo"):
+                if line.lower().startswith(("model name", "cpu part")):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except OSError:
+            pass
+    return {"nproc": os.cpu_count(), "cpu_model": model or "unknown", "machine": platform.machine()}
 
 
 class ClockSampler:
@@ -128,7 +180,7 @@ class ClockSampler:
                 ["nvidia-smi", "-i", str(gpu_index),
                  "--query-gpu=clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
                  "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-                 "clocks_event_reasons.sw_power_cap",
+                 "clocks_event_reasons.sw_power_cap,utilization.gpu",
                  "--format=csv,noheader,nounits", "-lms", str(period_ms)],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except Exception:
@@ -142,41 +194,53 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
-        sm, mx, reasons = [], [], set()
+        sm, mx, busy, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in open(self.path):
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 7:
+            if len(parts) < 8:
                 continue
             try:
-                sm.append(float(parts[0]))
-                mx.append(float(parts[1]))
+                f_sm, f_mx = float(parts[0]), float(parts[1])
             except ValueError:
                 continue
+            sm.append(f_sm)
+            mx.append(f_mx)
+            try:
+                busy.append(float(parts[7]) > 0)
+            except ValueError:
+                busy.append(False)
             for n, v in zip(names, parts[3:7]):
                 if v.lower() == "active":
                     reasons.add(n)
         os.unlink(self.path)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        loaded = [s for s, b in zip(sm, busy) if b]
+        return {"sm_mhz": statistics.median(loaded or sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm), "samples_under_load": len(loaded),
+                "period_ms": 50}
 
 
 def workload_config(wl: W.Workload) -> dict:
-    """The keys that name the workload, shared by both arms."""
+    """The keys that name the workload; both arms print exactly this dict."""
     return {"workload": wl.name, "num_reqs": wl.num_reqs, "total_tokens": wl.total_tokens,
             "block_size": wl.block_size, "entry_size": wl.entry_size, "num_blocks": wl.num_blocks,
-            "cache_dtype": wl.src_dtype, "out_dtype": wl.dst_dtype, "bytes_per_step": wl.algorithmic_bytes()}
+            "cache_dtype": wl.src_dtype, "out_dtype": wl.dst_dtype, "bytes_per_step": wl.algorithmic_bytes(),
+            "l2": L2_POLICY}
 
 
 def make_workload(name: str) -> W.Workload:
     return W.CONFIGS[name]()
 
 
+def dtype_label(wl: W.Workload) -> str:
+    return wl.src_dtype if wl.src_dtype == wl.dst_dtype else f"{wl.src_dtype}->{wl.dst_dtype}"
+
+
 class DeviceInputs:
     """One replica of a workload's inputs and output, resident on the device."""
 
-    def __init__(self, wl: W.Workload, device):
-        self.cache_full = wl.cache.to(device)
+    def __init__(self, wl: W.Workload, device, cache=None):
+        self.cache_full = wl.cache.to(device) if cache is None else cache
         self.cache = self.cache_full[:, :, :wl.entry_size]
         self.bt = wl.block_table.to(device)
         self.cu = wl.cu_seq_lens.to(device)
@@ -189,148 +253,236 @@ class DeviceInputs:
         return self.cache_full.numel() * self.cache_full.element_size() + self.dst.numel() * self.dst.element_size()
 
 
+class Runner:
+    """A workload on the device: replicas, one scheduling workspace, the call."""
+
+    def __init__(self, wl: W.Workload, dev, stream, args):
+        from paged_mla_kv_cache_gb300 import binding
+        self.binding = binding
+        self.wl, self.dev, self.stream, self.args = wl, dev, stream, args
+        base = DeviceInputs(wl, dev)
+        self.nrep = max(2, math.ceil(4 * L2_BYTES / base.nbytes()))
+        self.reps = [base] + [DeviceInputs(wl, dev) for _ in range(self.nrep - 1)]
+        self.ws_buf = None if args.no_workspace else binding.new_workspace(dev)
+        if args.entry == "tokens":
+            # the per-token entry point: each output row names its request
+            cu_h = wl.cu_seq_lens.numpy()
+            t2s_h = np.full(wl.total_tokens, -1, np.int32)
+            for r in range(wl.num_reqs):
+                t2s_h[cu_h[r]:min(cu_h[r + 1], wl.total_tokens)] = r
+            for r in self.reps:
+                r.t2s = torch.from_numpy(t2s_h).to(dev)
+        path, _ = binding.select_path(base.cache, base.dst, base.bt, base.cu, num_reqs=wl.num_reqs,
+                                      options=args.options)
+        self.path = ("per-token " + path) if args.entry == "tokens" else path
+
+    def footprint_mb(self):
+        return sum(r.nbytes() for r in self.reps) / 1e6
+
+    def step(self, k, strm=None, options=None):
+        r = self.reps[k % self.nrep]
+        b = self.binding
+        opts = self.args.options if options is None else options
+        s = self.stream if strm is None else strm
+        if self.args.entry == "tokens":
+            b.gather_tokens(r.cache, r.dst, r.bt, r.t2s, r.cu, r.scale, r.err, num_reqs=self.wl.num_reqs,
+                            stream=s, options=opts, workspace=self.ws_buf)
+        else:
+            b.gather(r.cache, r.dst, r.bt, r.cu, r.ss, r.scale, r.err, num_reqs=self.wl.num_reqs,
+                     stream=s, options=opts, workspace=self.ws_buf)
+
+    def capture(self, n, options=None):
+        """A CUDA graph of n consecutive steps (our launches only)."""
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            cs = torch.cuda.current_stream()
+            for k in range(n):
+                self.step(k, cs, options)
+        return g
+
+    def graphs_for(self, steps, options=None):
+        per_graph = min(steps, self.nrep * max(1, 120 // self.nrep))
+        n_main, rem = divmod(steps, per_graph)
+        g_main = self.capture(per_graph, options)
+        g_rem = self.capture(rem, options) if rem else None
+        g_main.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        torch.cuda.synchronize(self.dev)
+        return g_main, n_main, g_rem
+
+    def timed_region(self, graphs, world):
+        """One region of exactly the graphs' steps, events on our stream,
+        barrier + synchronize on both sides. Returns ms (max over ranks)."""
+        g_main, n_main, g_rem = graphs
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(self.dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(self.stream)
+        for _ in range(n_main):
+            g_main.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        b.record(self.stream)
+        torch.cuda.synchronize(self.dev)
+        if world > 1:
+            torch.distributed.barrier()
+        return reduce_max(a.elapsed_time(b), self.dev)
+
+    def cold(self, iters=30, read_back=False):
+        """Median call time with L2 flushed before each call, outside the event
+        pair: a 512 MB buffer is written (the page's cold-cache protocol), and
+        with read_back it is then read back too, so that L2 holds clean lines
+        of another buffer and no write-back of the flush lands in the call."""
+        flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=self.dev)
+        sink = torch.empty((), dtype=torch.int64, device=self.dev)
+        times = []
+        for k in range(iters):
+            flush.fill_(k & 0xFF)
+            if read_back:
+                torch.sum(flush.view(torch.int64), dim=0, out=sink)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(self.stream)
+            self.step(k)
+            b.record(self.stream)
+            torch.cuda.synchronize(self.dev)
+            times.append(a.elapsed_time(b))
+        del flush
+        times.sort()
+        med = statistics.median(times)
+        alg = self.wl.algorithmic_bytes()
+        peak, _ = measured_peak()
+        return {"median_us": round(med * 1e3, 2), "p10_us": round(times[len(times) // 10] * 1e3, 2),
+                "p90_us": round(times[(9 * len(times)) // 10] * 1e3, 2), "iters": iters,
+                "gbs": round(alg / (med * 1e-3) / 1e9, 1), "frac": round(alg / (med * 1e-3) / 1e9 / peak, 4),
+                "flush": ("512 MB written then read back" if read_back else "512 MB written")
+                         + " before each call, outside the event pair"}
+
+    def check_flags(self):
+        for r in self.reps:
+            flag = int(r.err.item())
+            if flag != 0:
+                raise RuntimeError(f"{self.wl.name}: gather reported data errors (flag {flag}) on valid inputs")
+
+    def close(self):
+        del self.reps
+        torch.cuda.empty_cache()
+
+
+def steady(runner: Runner, steps: int, world: int, min_total_ms: float = 0.0, max_repeats: int = 1,
+           options=None):
+    """Median over repeats of a region of exactly `steps` steps."""
+    graphs = runner.graphs_for(steps, options)
+    regions = [runner.timed_region(graphs, world)]
+    want = 1 if max_repeats <= 1 else max(5, min(max_repeats, math.ceil(min_total_ms / max(regions[0], 1e-6))))
+    while len(regions) < want:
+        regions.append(runner.timed_region(graphs, world))
+    del graphs
+    return regions
+
+
+def run_per_config(args, dev, stream, world, headline=None):
+    """Steady state and cold figures for every named target workload."""
+    peak, _ = measured_peak()
+    out = {}
+    for name in PER_CONFIG:
+        if headline is not None and name == args.config:
+            out[name] = headline
+            continue
+        wl = make_workload(name)
+        r = Runner(wl, dev, stream, args)
+        for k in range(max(args.warmup, 3)):
+            r.step(k)
+        torch.cuda.synchronize(dev)
+        alg = wl.algorithmic_bytes()
+        # about 30 ms of steps per region, median of 5 regions
+        est = alg / (peak * 0.8e9) * 1e3
+        n = int(min(3000, max(30, 30.0 / est)))
+        regions = steady(r, n, world, max_repeats=5, min_total_ms=0.0)
+        ms = statistics.median(regions) / n
+        cold = r.cold()
+        cold_clean = r.cold(read_back=True)
+        r.check_flags()
+        out[name] = {"workload": wl.name, "bytes_per_step": alg, "dtype": dtype_label(wl), "path": r.path,
+                     "steady": {"gbs": round(alg / (ms * 1e-3) / 1e9, 1),
+                                "frac": round(alg / (ms * 1e-3) / 1e9 / peak, 4),
+                                "per_launch_us": round(ms * 1e3, 2), "steps_per_region": n,
+                                "regions": len(regions)},
+                     "cold": cold, "cold_clean": cold_clean}
+        r.close()
+        del wl
+    return out
+
+
 def run_ours(args, wl: W.Workload, ws: int, rank: int, local: int):
-    from paged_mla_kv_cache_gb300 import binding
     from paged_mla_kv_cache_gb300.build import build_library
     build_library()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream(dev)
     alg_bytes = wl.algorithmic_bytes()
-
-    base = DeviceInputs(wl, dev)
-    nrep = max(2, math.ceil(4 * L2_BYTES / base.nbytes()))
-    reps = [base] + [DeviceInputs(wl, dev) for _ in range(nrep - 1)]
-
-    # one scheduling workspace serves every call on this stream
-    ws_buf = None if args.no_workspace else binding.new_workspace(dev)
-
-    if args.entry == "tokens":
-        # the per-token entry point: each output row names its request
-        cu_h = wl.cu_seq_lens.numpy()
-        t2s_h = np.full(wl.total_tokens, -1, np.int32)
-        for r in range(wl.num_reqs):
-            t2s_h[cu_h[r]:min(cu_h[r + 1], wl.total_tokens)] = r
-        for r in reps:
-            r.t2s = torch.from_numpy(t2s_h).to(dev)
-
-    def step(k, strm=None, options=None):
-        r = reps[k % nrep]
-        opts = args.options if options is None else options
-        if args.entry == "tokens":
-            binding.gather_tokens(r.cache, r.dst, r.bt, r.t2s, r.cu, r.scale, r.err, num_reqs=wl.num_reqs,
-                                  stream=stream if strm is None else strm, options=opts, workspace=ws_buf)
-        else:
-            binding.gather(r.cache, r.dst, r.bt, r.cu, r.ss, r.scale, r.err, num_reqs=wl.num_reqs,
-                           stream=stream if strm is None else strm, options=opts, workspace=ws_buf)
-
-    path, unit = binding.select_path(base.cache, base.dst, base.bt, base.cu, num_reqs=wl.num_reqs,
-                                     options=args.options)
-    if args.entry == "tokens":
-        path = "per-token " + ("SIMT" if path != "bulk" else "bulk")
+    runner = Runner(wl, dev, stream, args)
     for k in range(args.warmup):
-        step(k)
+        runner.step(k)
     torch.cuda.synchronize(dev)
 
-    # The timed steps are replayed from CUDA graphs of our launches so that the
-    # host's per-call cost (argument marshalling, launch) stays off the clock.
-    def capture(n, options=None):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            cs = torch.cuda.current_stream()
-            for k in range(n):
-                step(k, cs, options)
-        return g
-
-    per_graph = min(args.steps, nrep * max(1, 120 // nrep))
-    g_main = capture(per_graph)
-    n_main, rem = divmod(args.steps, per_graph)
-    g_rem = capture(rem) if rem else None
-    g_main.replay()
-    torch.cuda.synchronize(dev)
-    if ws > 1:
-        torch.distributed.barrier()
-
-    # --- timed region: K steps -----------------------------------------------
+    # --- timed regions: exactly K steps each, repeated so that the clock
+    # sampler (50 ms period) sees the GPU under load --------------------------
+    graphs = runner.graphs_for(args.steps)
+    runner.timed_region(graphs, ws)  # untimed: settles the replays
     sampler = ClockSampler(local)
     time.sleep(0.15)  # let the sampler start
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    if ws > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize(dev)
-    start.record(stream)
-    for _ in range(n_main):
-        g_main.replay()
-    if g_rem is not None:
-        g_rem.replay()
-    end.record(stream)
-    torch.cuda.synchronize(dev)
-    if ws > 1:
-        torch.distributed.barrier()
+    regions = [runner.timed_region(graphs, ws)]
+    repeats = max(3, min(args.max_repeats, math.ceil(args.min_timed_ms / max(regions[0], 1e-6))))
+    while len(regions) < repeats:
+        regions.append(runner.timed_region(graphs, ws))
     clocks = sampler.stop()
-    ms = reduce_max(start.elapsed_time(end), dev)
-    for r in reps:
-        flag = int(r.err.item())
-        if flag != 0:
-            raise RuntimeError(f"gather reported data errors (flag {flag}) on valid inputs")
-
+    del graphs
+    runner.check_flags()
+    ms = statistics.median(regions)
     ms_per_step = ms / args.steps
     value = weak_value(alg_bytes, args.steps, ms, ws)
     # the gather is the only kernel of a step: its average launch duration is
-    # the timed region over the steps (inter-launch gaps included)
+    # the region over the steps (inter-launch gaps included)
     per_launch_ms = ms_per_step
 
     # --- the same steps with the early-metadata promise (reported beside) -----
     early = None
     if not args.quick and args.entry == "gather" and not (args.options & 8):
-        opts = args.options | 8
-        n_e = min(args.steps, 3000)
-        pg = min(n_e, per_graph)
-        g_e = capture(pg, opts)
-        g_e.replay()
-        torch.cuda.synchronize(dev)
-        reps_e = max(1, n_e // pg)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(reps_e):
-            g_e.replay()
-        b.record(stream)
-        torch.cuda.synchronize(dev)
-        ms_e = reduce_max(a.elapsed_time(b), dev)
-        steps_e = reps_e * pg
-        v_e = weak_value(alg_bytes, steps_e, ms_e, ws)
+        n_e = min(max(args.steps, 200), 3000)
+        reg = steady(runner, n_e, ws, options=args.options | 8)
+        ms_e = reg[0]
         peak_e, _ = measured_peak()
-        early = {"value": round(v_e, 1), "unit": "GB/s", "frac": round(alg_bytes / (ms_e / steps_e * 1e-3) / 1e9 / peak_e, 4),
-                 "per_launch_us": round(ms_e / steps_e * 1e3, 2), "steps": steps_e,
+        early = {"value": round(weak_value(alg_bytes, n_e, ms_e, ws), 1), "unit": "GB/s",
+                 "frac": round(alg_bytes / (ms_e / n_e * 1e-3) / 1e9 / peak_e, 4),
+                 "per_launch_us": round(ms_e / n_e * 1e3, 2), "steps": n_e,
                  "options": "PMG_OPT_EARLY_METADATA (caller promises no running kernel writes the metadata)"}
-        del g_e
 
-    # --- cold: flush L2 (write 512 MB) before each call, median -------------
-    cold = None
-    if not args.quick:
-        flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
-        times = []
-        for k in range(30):
-            flush.fill_(k & 0xFF)
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            step(k)
-            b.record(stream)
-            torch.cuda.synchronize(dev)
-            times.append(a.elapsed_time(b))
-        med = statistics.median(times)
-        cold = {"median_us": round(med * 1e3, 2), "gbs": round(alg_bytes / (med * 1e-3) / 1e9, 1),
-                "flush": "512 MB write before each call"}
-        del flush
+    cold = None if args.quick else runner.cold()
+    cold_clean = None if args.quick else runner.cold(read_back=True)
+    peak, peak_kind = measured_peak()
+    achieved = alg_bytes / (per_launch_ms * 1e-3) / 1e9
+    headline_entry = {"workload": wl.name, "bytes_per_step": alg_bytes, "dtype": dtype_label(wl),
+                      "path": runner.path,
+                      "steady": {"gbs": round(achieved, 1), "frac": round(achieved / peak, 4),
+                                 "per_launch_us": round(per_launch_ms * 1e3, 2), "steps_per_region": args.steps,
+                                 "regions": len(regions)},
+                      "cold": cold, "cold_clean": cold_clean}
+    footprint = runner.footprint_mb()
+    nrep = runner.nrep
+    runner.close()
+
+    per_config = None
+    if not args.quick and rank == 0 and not args.no_per_config:
+        per_config = run_per_config(args, dev, stream, 1, headline=headline_entry)
 
     # --- end to end: host buffers through the public binding -----------------
     e2e = None
     if not args.quick:
-        e2e = run_e2e(wl, dev, stream, alg_bytes, steps=min(max(args.steps // 200, 5), 40), ws=ws)
+        e2e = run_e2e(wl, dev, stream, alg_bytes, steps=20, ws=ws)
 
-    peak, peak_kind = measured_peak()
-    achieved = alg_bytes / (per_launch_ms * 1e-3) / 1e9
+    traffic = profiled_traffic(args.config) if args.entry == "gather" and args.options == 0 else None
     result = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -342,30 +494,41 @@ def run_ours(args, wl: W.Workload, ws: int, rank: int, local: int):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16" if wl.src_dtype == wl.dst_dtype == "bf16" else f"{wl.src_dtype}->{wl.dst_dtype}",
+        "dtype": dtype_label(wl),
         "data": "synthetic (seeded N(0,1) cache, seeded block-id permutation)",
-        "config": {
-            **workload_config(wl),
-            "path": path if args.options == 0 else f"{path} (options {args.options})",
-            "schedule": ("static" if args.no_workspace else "dynamic (workspace)")
-                        + (", early metadata" if args.early_metadata else ""),
-            "l2": f"{nrep} rotating input replicas ({sum(r.nbytes() for r in reps) / 1e6:.0f} MB) > 4x L2; no flush",
-            "parallelism": f"replicas x{ws}",
-        },
+        "config": workload_config(wl),
+        "path": runner.path if args.options == 0 else f"{runner.path} (options {args.options})",
+        "schedule": ("static" if args.no_workspace else "dynamic (workspace)")
+                    + (", early metadata" if args.early_metadata else ""),
+        "parallelism": f"replicas x{ws}",
+        "timing": {"regions": len(regions), "steps_per_region": args.steps,
+                   "region_ms": {"min": round(min(regions), 4), "median": round(ms, 4), "max": round(max(regions), 4)},
+                   "mean_value": round(weak_value(alg_bytes, args.steps * len(regions), sum(regions), ws), 1),
+                   "replicas": f"{nrep} input replicas ({footprint:.0f} MB)",
+                   "how": "value = bytes x K / median over regions of the device time of exactly K steps "
+                          "(CUDA events on the launching stream, barrier + synchronize on both sides)"},
         "roofline": {
             "bound": "hbm",
             "achieved": round(achieved, 1),
             "peak": peak,
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
-            "traffic": profiled_traffic(args.config),
-            "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
+            "traffic": None if traffic is None else traffic["read"] + traffic["write"],
+            "traffic_read": None if traffic is None else traffic["read"],
+            "traffic_write": None if traffic is None else traffic["write"],
+            "traffic_source": None if traffic is None else traffic["source"],
+            "algorithmic_bytes": alg_bytes,
+            "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, burst copy)" if peak_kind == "measured"
+                           else "fallback",
             "per_launch_us": round(per_launch_ms * 1e3, 2),
         },
         "clocks": clocks,
         "gpu_launches": args.steps,
+        "gpu_launches_note": "our kernel launches inside one timed region (one per step)",
         "cold": cold,
+        "cold_clean": cold_clean,
         "early_metadata": early,
+        "per_config": per_config,
         "e2e": e2e,
     }
     return result
@@ -414,14 +577,16 @@ def run_e2e(wl, dev, stream, alg_bytes, steps, ws):
     b.record(stream)
     torch.cuda.synchronize(dev)
     ms = a.elapsed_time(b) / steps
+    if int(d_err.item()) != 0:
+        raise RuntimeError("e2e: gather reported data errors on valid inputs")
     return {"value": round(ws * alg_bytes / (ms * 1e-3) / 1e9, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4), "steps": steps}
 
 
-def oracle_sample(wl: W.Workload, rows: int):
-    """A bounded sample of the workload for the CPU oracle: the first `rows`
-    output rows of each request's share, as one smaller call of the same shape."""
-    from oracle import gather as og
+def sample_call(wl: W.Workload, rows: int):
+    """A bounded sample of the workload for the CPU oracle: the first
+    ceil(len_r * rows / total) rows of every request, as one smaller call of the
+    same shape. Returns (args for oracle.gather, bytes, rows)."""
     cache = W.tensor_bits(wl.cache)
     cache_view = np.lib.stride_tricks.as_strided(
         cache, shape=(cache.shape[0], cache.shape[1], wl.entry_size), strides=cache.strides)
@@ -429,37 +594,86 @@ def oracle_sample(wl: W.Workload, rows: int):
     lens = [int(math.ceil(L * frac)) for L in wl.lens]
     cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
     T = int(cu[-1])
-    dst = wl.new_dst(row_stride=None)[:T] if T <= wl.total_tokens else None
     bt = wl.block_table.numpy()
     ss = None if wl.seq_starts is None else wl.seq_starts.numpy()
-    sample_bytes = T * wl.entry_size * (W.ELEM_BYTES[wl.src_dtype] + W.ELEM_BYTES[wl.dst_dtype])
-
-    def run():
-        return og.gather(cache_view, bt, cu, ss, wl.num_reqs, T, wl.block_size, wl.entry_size, wl.src_dtype,
-                         wl.dst_dtype, wl.scale, dst)
-    return run, sample_bytes, T
+    nbytes = T * wl.entry_size * (W.ELEM_BYTES[wl.src_dtype] + W.ELEM_BYTES[wl.dst_dtype])
+    return dict(cache=cache_view, bt=bt, cu=cu, ss=ss, T=T), nbytes, T
 
 
-def cpu_baseline(wl: W.Workload, budget_s: float = 10.0):
-    """The oracle as it stands, single-threaded on a host core, repeated over the
-    full workload (or a prefix sample if one call would exceed the budget)."""
-    run, nbytes, rows = oracle_sample(wl, wl.rows)
-    t0 = time.perf_counter()
-    run()
-    t1 = time.perf_counter() - t0
-    if t1 > budget_s / 3:
-        run, nbytes, rows = oracle_sample(wl, int(wl.rows * budget_s / 3 / t1))
+def split_rows(call: dict, parts: int):
+    """The sample call cut into `parts` calls over disjoint output row ranges
+    (each a plain oracle call: the requests overlapping the range, their row
+    ranges clipped and their starts advanced by the rows cut off)."""
+    cu, T = call["cu"].astype(np.int64), call["T"]
+    R = len(cu) - 1
+    ss = np.zeros(R, np.int64) if call["ss"] is None else call["ss"].astype(np.int64)
+    out = []
+    bounds = np.linspace(0, T, parts + 1).astype(np.int64)
+    for a, b in zip(bounds[:-1], bounds[1:]):
+        if b <= a:
+            continue
+        rs = [r for r in range(R) if cu[r] < b and cu[r + 1] > a]
+        c_lo = np.array([max(cu[r], a) for r in rs], np.int64)
+        c_hi = np.array([min(cu[r + 1], b) for r in rs], np.int64)
+        sub_cu = np.concatenate([[0], np.cumsum(c_hi - c_lo)]).astype(np.int32)
+        sub_ss = np.array([ss[r] + (c_lo[i] - cu[r]) for i, r in enumerate(rs)], np.int32)
+        out.append(dict(cache=call["cache"], bt=np.ascontiguousarray(call["bt"][rs]), cu=sub_cu, ss=sub_ss,
+                        T=int(b - a), row0=int(a)))
+    return out
+
+
+def oracle_runner(wl: W.Workload, call: dict):
+    from oracle import gather as og
+    dst = wl.new_dst()[:call["T"]] if call["T"] <= wl.total_tokens else None
+
+    def run(c=call, d=dst):
+        return og.gather(c["cache"], c["bt"], c["cu"], c["ss"], len(c["cu"]) - 1, c["T"], wl.block_size,
+                         wl.entry_size, wl.src_dtype, wl.dst_dtype, wl.scale, d)
+    return run
+
+
+def time_oracle(run, budget_s):
     n, t0 = 0, time.perf_counter()
     while True:
         run()
         n += 1
         el = time.perf_counter() - t0
         if el >= budget_s or (n >= 3 and el >= budget_s / 2 and el / n * (n + 1) > budget_s):
-            break
+            return n, el
+
+
+def cpu_baseline(wl: W.Workload, budget_s: float = 10.0):
+    """The oracle as it stands on the host cores: single-threaded, repeated over
+    the full workload (or a prefix sample if one call would exceed a third of
+    the budget); then the same sample as concurrent oracle calls over disjoint
+    row ranges, one per core (the oracle's C loop runs outside the GIL)."""
+    facts = cpu_facts()
+    call, nbytes, rows = sample_call(wl, wl.rows)
+    run = oracle_runner(wl, call)
+    t0 = time.perf_counter()
+    run()
+    t1 = time.perf_counter() - t0
+    if t1 > budget_s / 3:
+        call, nbytes, rows = sample_call(wl, int(wl.rows * budget_s / 3 / t1))
+        run = oracle_runner(wl, call)
+    n, el = time_oracle(run, budget_s)
     gbs = nbytes * n / el / 1e9
-    return {"value": round(gbs, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{n} full oracle calls over {rows} of {wl.rows} rows in {el:.1f} s "
-                      f"({platform.machine()}, single thread)"}
+    res = {"value": round(gbs, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+           "sample": f"{n} oracle calls over {rows} of {wl.rows} rows in {el:.1f} s, single thread",
+           **facts}
+    cores = facts["nproc"] or 1
+    if cores > 1:
+        parts = split_rows(call, cores)
+        runs = [oracle_runner(wl, c) for c in parts]
+        with concurrent.futures.ThreadPoolExecutor(max_workers=len(runs)) as pool:
+            def all_parts():
+                list(pool.map(lambda f: f(), runs))
+            m, el_m = time_oracle(all_parts, budget_s / 2)
+        res["all_cores"] = {"value": round(nbytes * m / el_m / 1e9, 3), "unit": "GB/s", "cores": len(runs),
+                            "kind": f"oracle, {len(runs)} cores",
+                            "sample": f"{m} passes over the same {rows} rows split into {len(runs)} concurrent "
+                                      f"oracle calls (disjoint row ranges) in {el_m:.1f} s"}
+    return res
 
 
 def run_reference(args, wl, ws, rank):
@@ -467,14 +681,16 @@ def run_reference(args, wl, ws, rank):
     sample of the workload so that warmup + steps end within a few minutes."""
     if rank != 0:
         return None
-    run_full, nbytes_full, _ = oracle_sample(wl, wl.rows)
+    call, _, _ = sample_call(wl, wl.rows)
+    run_full = oracle_runner(wl, call)
     t0 = time.perf_counter()
     run_full()
     t_full = time.perf_counter() - t0
     budget = 90.0
     per_step = budget / max(args.steps + args.warmup, 1)
     rows = max(64, min(wl.rows, int(wl.rows * per_step / max(t_full, 1e-9))))
-    run, nbytes, rows = oracle_sample(wl, rows)
+    call, nbytes, rows = sample_call(wl, rows)
+    run = oracle_runner(wl, call)
     for _ in range(args.warmup):
         run()
     t0 = time.perf_counter()
@@ -482,14 +698,17 @@ def run_reference(args, wl, ws, rank):
         run()
     el = time.perf_counter() - t0
     value = nbytes * args.steps / el / 1e9
-    sample = f"{rows} of {wl.rows} rows per step ({platform.machine()}, single thread)"
+    facts = cpu_facts()
+    sample = f"{rows} of {wl.rows} rows per step (prefix of every request), single thread"
     return {
         "impl": "reference",
         "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": wl.src_dtype, "data": "synthetic",
-        "config": {**workload_config(wl), "path": "CPU oracle (per-token loop)"},
-        "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "scaling": "weak", "vs_baseline": None, "dtype": dtype_label(wl), "data": "synthetic",
+        "config": workload_config(wl),
+        "path": "CPU oracle (per-token loop)",
+        "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample,
+                         **facts},
         "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -497,11 +716,16 @@ def run_reference(args, wl, ws, rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
-    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default="60k", choices=sorted(W.CONFIGS))
-    ap.add_argument("--quick", action="store_true", help="skip the cold, e2e and CPU-baseline legs")
+    ap.add_argument("--config", default=HEADLINE, choices=sorted(W.CONFIGS))
+    ap.add_argument("--quick", action="store_true",
+                    help="skip the per-config, cold, early-metadata, e2e and CPU-baseline legs")
+    ap.add_argument("--no-per-config", action="store_true", help="skip the per-config leg only")
+    ap.add_argument("--min-timed-ms", type=float, default=600.0,
+                    help="repeat the K-step region until the regions add up to this much device time")
+    ap.add_argument("--max-repeats", type=int, default=400)
     ap.add_argument("--options", type=int, default=0, help="PMG_OPT_* bits passed to every call (path sweeps)")
     ap.add_argument("--early-metadata", action="store_true",
                     help="pass PMG_OPT_EARLY_METADATA (the caller's promise that no running kernel writes the "
@@ -513,6 +737,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.steps < 1:
+        ap.error("--steps must be >= 1")
     if args.early_metadata:
         args.options |= 8  # PMG_OPT_EARLY_METADATA
     ws, rank, local = dist_env()
@@ -520,10 +746,10 @@ def main():
         backend = "nccl" if args.impl == "ours" else "gloo"
         torch.distributed.init_process_group(backend=backend, device_id=torch.device("cuda", local)
                                              if backend == "nccl" else None)
-    wl = make_workload(args.config)
     if args.impl == "reference":
-        res = run_reference(args, wl, ws, rank)
+        res = run_reference(args, make_workload(args.config), ws, rank) if rank == 0 else None
     else:
+        wl = make_workload(args.config)
         res = run_ours(args, wl, ws, rank, local)
         if rank == 0 and not args.quick:
             res["cpu_baseline"] = cpu_baseline(wl)

@@ -183,11 +183,12 @@ int pmg_gather_ex(const void* cache, int64_t cache_block_stride, int64_t cache_t
  * pmg_gather_ex, for callers that cannot allocate device memory. The pages
  * have no counterpart of this entry point.
  *
- * Who needs it: code that may not call cudaMalloc, such as a serving engine
- * that reserves nearly all of HBM for its own KV-cache pool up front, code
- * running inside a CUDA stream capture (an allocation is not a stream operation
- * and cannot be captured), or a latency-bound path that cannot afford
- * cudaMalloc's implicit device synchronisation.
+ * Who needs it: callers that may not call cudaMalloc. A serving engine that
+ * reserves nearly all of HBM for its own KV-cache pool at start-up leaves no
+ * room for, and often forbids, allocations outside that pool; a caller on a
+ * latency-bound path cannot afford cudaMalloc's implicit device
+ * synchronisation; and a plugin inside a host framework that owns every
+ * allocation may only use memory handed to it.
  *
  * The arguments, their meaning and the results are those of pmg_gather; the
  * caller still passes every input and output. Instead of a caller workspace,
@@ -206,6 +207,16 @@ int pmg_gather_ex(const void* cache, int64_t cache_block_stride, int64_t cache_t
  * it and may produce wrong output; serialise them, or use pmg_gather_ex with a
  * workspace per stream.
  */
+
+/*
+ * pmg_debug_noalloc_scratch — test hook: the device address of the static
+ * scratch pmg_gather_noalloc uses on the current device, and its size in
+ * int32 elements. Like the first pmg_gather_noalloc call it performs the
+ * one-time address lookup for the device. Tests use it to leave stale values
+ * in the array and check that a call still starts from a cleared counter.
+ * Writing to the array while a pmg_gather_noalloc call runs corrupts that call.
+ */
+int pmg_debug_noalloc_scratch(void** device_ptr, int64_t* num_ints);
 int pmg_gather_noalloc(const void* cache, int64_t cache_block_stride, int64_t cache_token_stride,
                        int64_t num_blocks, const int32_t* block_table, int64_t block_table_stride,
                        const int32_t* cu_seq_lens, const int32_t* seq_starts, int32_t num_reqs,

@@ -78,6 +78,8 @@ def load_library() -> ctypes.CDLL:
         L.pmg_gather_ex.argtypes = gather_args[:18] + [vp, vp, u32]
         L.pmg_gather_noalloc.restype = ctypes.c_int
         L.pmg_gather_noalloc.argtypes = gather_args
+        L.pmg_debug_noalloc_scratch.restype = ctypes.c_int
+        L.pmg_debug_noalloc_scratch.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(i64)]
         L.pmg_gather_tokens.restype = ctypes.c_int
         L.pmg_gather_tokens.argtypes = [vp, i64, i64, i64, vp, i64, vp, vp, i32, i64, i32, i32, i32, i32, vp, vp, i64,
                                         vp, vp, vp, u32]
@@ -180,6 +182,18 @@ def gather_noalloc(cache: torch.Tensor, dst: torch.Tensor, block_table: torch.Te
         _ptr(dst), dst.stride(0), _ptr(error_flag), _stream_handle(stream))
     if st != PMG_OK:
         raise PmgError(st, "pmg_gather_noalloc")
+
+
+def debug_noalloc_scratch() -> Tuple[int, int]:
+    """(device address, int32 elements) of the static scratch that
+    gather_noalloc uses on the current device (pmg_debug_noalloc_scratch); a
+    test hook."""
+    ptr = ctypes.c_void_p()
+    n = ctypes.c_int64()
+    st = load_library().pmg_debug_noalloc_scratch(ctypes.byref(ptr), ctypes.byref(n))
+    if st != PMG_OK:
+        raise PmgError(st, "pmg_debug_noalloc_scratch")
+    return int(ptr.value), int(n.value)
 
 
 def gather_tokens(cache: torch.Tensor, dst: torch.Tensor, block_table: torch.Tensor, token_to_seq: torch.Tensor,

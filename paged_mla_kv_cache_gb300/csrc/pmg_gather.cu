@@ -105,6 +105,7 @@ struct Params {
   const int32_t* gate;    // large batches: non-zero when cu_seq_lens failed validation (write nothing)
   int32_t early;          // plan and first block ids before the previous grid completes (caller's promise)
   int32_t spec;           // plan and first batch before the previous grid completes, checked after it
+  int32_t spec_guess;     // speculative start of one request without seq_starts: assume cu = [0, T]
   int32_t prefetch_rows;  // rows of the pre-wait batch warmed in L2
   const int32_t* t2s;     // per-token gather: request of each output row (token mode)
   int32_t token_mode;     // 1: rows [0, T) map through t2s instead of the page plan
@@ -336,6 +337,27 @@ __device__ int build_plan(const Params& p, const PlanView& v, bool report_flags,
   if (any_bad_start && report_flags && tid == 0) set_flag(p, PMG_FLAG_SEQ_START);
   if (flags_out != nullptr) *flags_out = any_bad_start ? PMG_FLAG_SEQ_START : 0;
   return total;
+}
+
+// The plan of a single request without seq_starts whose cu_seq_lens is
+// [0, T] (or [0] with the implied end): the usual form of a one-request call,
+// written without reading anything. The speculative start uses it as its
+// guess; the check after the previous grid completes reads cu_seq_lens and
+// compares it with raw_cu, so a call whose cu_seq_lens differs replans from
+// the real values.
+__device__ __forceinline__ int32_t guess_single_plan(const Params& p, const PlanView& v, int32_t* raw_cu) {
+  if ((threadIdx.x & 31) == 0) {
+    v.ob[0] = 0;
+    v.ob[1] = p.T;
+    v.st[0] = 0;
+    v.P[0] = 0;
+    v.P[1] = static_cast<int32_t>((static_cast<uint32_t>(p.T) + static_cast<uint32_t>(p.B) - 1u) /
+                                  static_cast<uint32_t>(p.B));
+    raw_cu[0] = 0;
+    raw_cu[1] = p.implied_end ? 0 : p.T;
+  }
+  __syncwarp();
+  return v.P[1];
 }
 
 // Before the previous grid is known to be done, a kernel may not read its
@@ -792,6 +814,12 @@ struct SegQueue {
   uint64_t empty[kSegBufs];
   int32_t tentative;  // batch 0 is the speculative first batch
   int32_t verdict;    // for it: 0 pending, 1 confirmed, 2 withdrawn
+  // The batch published before the previous grid completes, handed to a warp
+  // that warms L2 with its rows (the scheduler warp goes on to its check):
+  // pf_state 0 pending, 1 pf_seg holds pf_n segments, 2 nothing to warm.
+  Segment pf_seg[kSegCap];
+  int32_t pf_n;
+  int32_t pf_state;
 };
 
 __device__ __forceinline__ void segq_init(SegQueue& q) {
@@ -801,6 +829,26 @@ __device__ __forceinline__ void segq_init(SegQueue& q) {
   }
   q.tentative = 0;
   q.verdict = 0;
+  q.pf_state = 0;
+}
+
+// Scheduler warp: hands the batch just published in slot b to the warming warp.
+__device__ __forceinline__ void hand_off_prefetch(SegQueue& q, int b) {
+  const int lane = threadIdx.x & 31;
+  const int n = q.count[b];
+  if (lane < n) q.pf_seg[lane] = q.seg[b][lane];
+  if (lane == 0) q.pf_n = n;
+  __syncwarp();
+  if (lane == 0) {
+    __threadfence_block();
+    *reinterpret_cast<volatile int32_t*>(&q.pf_state) = 1;
+  }
+}
+
+// Scheduler warp, after the wait: nothing (more) will be handed off.
+__device__ __forceinline__ void pf_release(SegQueue& q) {
+  if ((threadIdx.x & 31) == 0 && *reinterpret_cast<volatile int32_t*>(&q.pf_state) == 0)
+    *reinterpret_cast<volatile int32_t*>(&q.pf_state) = 2;
 }
 
 // Verdict on the speculative first batch: 1 confirmed, 0 withdrawn, -1 the
@@ -823,13 +871,12 @@ __device__ __forceinline__ int spec_verdict(const SegQueue& q) {
 // the previous grid still writes those rows, the loads after the wait read
 // them as they are then, and rows of a withdrawn batch are only wasted
 // bandwidth. Every address is inside a row the batch's checks accepted.
-__device__ __forceinline__ void prefetch_batch(const Params& p, const SegQueue& q, int b, int32_t cap) {
+__device__ __forceinline__ void prefetch_rows(const Params& p, const Segment* segs, int n, int32_t cap) {
   const int lane = threadIdx.x & 31;
   const uint32_t rb = static_cast<uint32_t>(p.row_src_bytes);
   const uint32_t lpr = (rb + 127u) / 128u;  // lines a row touches from its start
-  const int n = q.count[b];
   for (int i = 0; i < n && cap > 0; ++i) {
-    const Segment sg = q.seg[b][i];
+    const Segment sg = segs[i];
     const int32_t rows = sg.nrows < cap ? sg.nrows : cap;
     cap -= rows;
     const uint32_t units = static_cast<uint32_t>(rows) * lpr;
@@ -841,6 +888,24 @@ __device__ __forceinline__ void prefetch_batch(const Params& p, const SegQueue& 
       asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
     }
   }
+}
+
+// The warming warp (a warp with nothing to do before the wait): waits, within
+// the bounded time, for the scheduler's hand-off and prefetches up to
+// p.prefetch_rows rows of the handed batch. Issuing the prefetches here keeps
+// them off the scheduler warp, whose check after the wait gates the first
+// stores.
+__device__ __forceinline__ void prefetch_helper(const Params& p, const SegQueue& q) {
+  const volatile int32_t* sp = &q.pf_state;
+  int32_t st = *sp;
+  if (st == 0) {
+    const uint64_t t0 = global_ns();
+    while ((st = *sp) == 0) {
+      if (global_ns() - t0 > kWaitLimitNs) return;
+    }
+  }
+  __threadfence_block();
+  if (st == 1 && p.prefetch_rows > 0) prefetch_rows(p, q.pf_seg, q.pf_n, p.prefetch_rows);
 }
 
 // The check of a speculative start (uses is 0): publishes the first batch
@@ -862,9 +927,10 @@ __device__ __forceinline__ bool spec_confirm(const Params& p, const PlanView& sv
     __syncwarp();
     if (lane == 0) mbar_arrive(&q.full[0]);
     uses = 1;
-    prefetch_batch(p, q, 0, p.prefetch_rows);
+    hand_off_prefetch(q, 0);
   }
   pdl_wait();
+  pf_release(q);
   const uint64_t keep = evict_last_policy();
   const int32_t phys_now = (publish && rd.idx >= 0) ? ld_meta(p.bt + rd.idx, keep) : 0;
   bool same = !publish || rd.idx < 0 || phys_now == rd.phys;
@@ -956,7 +1022,8 @@ __device__ bool run_scheduler(const Params& p, const PlanView& v, const PlanView
   } else if (p.spec) {
     raw_cu = sv.P + (p.R + 1);
     int plan_flags = 0;
-    const int32_t sn = build_plan<true>(p, sv, false, &plan_flags, raw_cu);
+    const int32_t sn = (p.spec_guess && p.R == 1 && p.ss == nullptr && p.T > 0) ? guess_single_plan(p, sv, raw_cu)
+                                                                  : build_plan<true>(p, sv, false, &plan_flags, raw_cu);
     if (sn > 0 && plan_flags == 0) {
       // the main loop resolves the first batch from this plan and checks both
       pv = sv;
@@ -964,14 +1031,20 @@ __device__ bool run_scheduler(const Params& p, const PlanView& v, const PlanView
       spec_first = true;
     } else {
       pdl_wait();
+      pf_release(q);
       num_tasks = build_plan<true>(p, v, blockIdx.x == 0);
     }
   }
-  Items its{};
+  if (!p.spec && !p.early) pf_release(q);
+  // the work items live in shared memory (only this warp reads them): fewer
+  // registers held across the loop
+  __shared__ Items its;
   bool have = false;
   if (num_tasks > 0) {
-    its = make_items(pv, p);
-    have = k < its.n;
+    const Items t = make_items(pv, p);
+    if (lane == 0) its = t;
+    __syncwarp();
+    have = k < t.n;
   }
   // with early metadata or a speculative start the workspace (claim counter)
   // is touched only after the previous grid is done: wait after the first
@@ -1003,9 +1076,10 @@ __device__ bool run_scheduler(const Params& p, const PlanView& v, const PlanView
             if (lane == 0) q.tentative = 1;
             (void)publish_tokens(p, q, uses, g0, srcs[0]);  // the first batch: no wait
             __syncwarp();
-            prefetch_batch(p, q, 0, p.prefetch_rows);
+            if (uses == 1) hand_off_prefetch(q, 0);
           }
           pdl_wait();
+          pf_release(q);
           const bool valid = __all_sync(0xffffffffu, tokens_unchanged<kTokGroup>(p, g0 + static_cast<uint32_t>(lane),
                                                                                    r1, rec));
           if (publish && lane == 0) *reinterpret_cast<volatile int32_t*>(&q.verdict) = valid ? 1 : 2;
@@ -1027,6 +1101,7 @@ __device__ bool run_scheduler(const Params& p, const PlanView& v, const PlanView
             // previous grid through a bounded wait. The wait (and this
             // item's claim) comes first.
             pdl_wait();
+            pf_release(q);
             waited = true;
             if (its.dynamic && lane == 0) claimed = gridDim.x + atomicAdd(reinterpret_cast<unsigned*>(p.sched), 1u);
           }
@@ -1061,6 +1136,7 @@ __device__ bool run_scheduler(const Params& p, const PlanView& v, const PlanView
         if (uses >= kSegBufs && !waited) {
           // as in token mode: no wait on the producer before the wait
           pdl_wait();
+          pf_release(q);
           waited = true;
           if (its.dynamic && lane == 0) claimed = gridDim.x + atomicAdd(reinterpret_cast<unsigned*>(p.sched), 1u);
         }
@@ -1071,7 +1147,7 @@ __device__ bool run_scheduler(const Params& p, const PlanView& v, const PlanView
         __syncwarp();
         if (lane == 0) mbar_arrive(&q.full[b]);
         ++uses;
-        if (!waited && uses == 1) prefetch_batch(p, q, b, p.prefetch_rows);  // early metadata
+        if (!waited && uses == 1) hand_off_prefetch(q, b);  // early metadata
         if (n < kSegCap) break;
         t += kSegCap;
       }
@@ -1092,13 +1168,17 @@ __device__ bool run_scheduler(const Params& p, const PlanView& v, const PlanView
       k = blockIdx.x;
       have = false;
       if (num_tasks > 0) {
-        its = make_items(pv, p);
-        have = k < its.n;
+        const Items t = make_items(pv, p);
+        __syncwarp();
+        if (lane == 0) its = t;
+        __syncwarp();
+        have = k < t.n;
       }
       continue;
     }
     if (!waited) {
       pdl_wait();
+      pf_release(q);
       waited = true;
       if (its.dynamic && lane == 0) claimed = gridDim.x + atomicAdd(reinterpret_cast<unsigned*>(p.sched), 1u);
     }
@@ -1115,6 +1195,7 @@ __device__ bool run_scheduler(const Params& p, const PlanView& v, const PlanView
     }
   }
   if (!waited) pdl_wait();
+  pf_release(q);
   const int b = static_cast<int>(uses % kSegBufs);
   if (uses >= kSegBufs && !mbar_wait_bounded(&q.empty[b], ((uses / kSegBufs) - 1u) & 1u)) return false;
   if (lane == 0) q.count[b] = -1;
@@ -1223,6 +1304,8 @@ __global__ void __launch_bounds__(kBulkThreads) gather_bulk_kernel(const __grid_
     if (p.token_mode) num_tasks = 1;
     else if (warp_plan && !p.spec) num_tasks = build_plan<true>(p, v, blockIdx.x == 0);
     if (!run_scheduler(p, v, sv, num_tasks, q)) set_flag(p, PMG_FLAG_TIMEOUT);
+  } else if (warp == 2) {
+    if (early) prefetch_helper(p, q);
   } else if (tid == 0) {
     if (early) pdl_wait();
     const uint64_t pol = evict_first_policy();
@@ -1627,7 +1710,10 @@ __global__ void __launch_bounds__(kCvtThreads) gather_tma_convert_kernel(const _
     }
   } else {
     // converters: every landed stage, unit u = (row, col) of the chunk
-    if (early) pdl_wait();
+    if (early) {
+      if (warp == 0) prefetch_helper(p, q);
+      pdl_wait();
+    }
     float scale = 1.0f;
     if (CONV == CONV_E4M3_BF16 || CONV == CONV_E4M3_F16 || CONV == CONV_E4M3_F32) {
       if (p.scale != nullptr) scale = __ldg(p.scale);
@@ -1929,6 +2015,13 @@ bool use_spec() {
   return v != 0;
 }
 
+// One request without seq_starts: the speculative plan assumes cu = [0, T]
+// instead of reading it (PMG_SPEC_GUESS=0 reads it, for A/B runs).
+bool use_spec_guess() {
+  static const int v = env_int("PMG_SPEC_GUESS", 1, 0, 1);
+  return v != 0;
+}
+
 int sched_min_rows() {
   static const int v = env_int("PMG_SCHED_MIN_ROWS", 32, 1, 1 << 30);
   return v;
@@ -2055,6 +2148,7 @@ int make_plan(const void* cache, int64_t cbs, int64_t cts, int64_t num_blocks, c
   // without the promise, small batches still plan before the wait and check
   // the plan after it (the TMA paths; the SIMT kernels ignore the field)
   q.spec = (!q.early && R <= kWarpPlanMaxReqs && use_spec()) ? 1 : 0;
+  q.spec_guess = use_spec_guess() ? 1 : 0;
   q.sched_static_pct = sched_static_pct();
   q.sched_min_rows = sched_min_rows();
   out.conv = conv;
@@ -2364,9 +2458,8 @@ int launch_gather(const Plan& pl, cudaStream_t stream) {
 // Scratch for pmg_gather_noalloc.
 //
 // Some callers cannot call cudaMalloc: a serving engine that hands nearly all
-// of HBM to its own KV-cache pool up front and lets nothing else allocate, code
-// that runs between the begin and end of a CUDA stream capture (an allocation is
-// not a stream operation and breaks or escapes the capture), and latency-bound
+// of HBM to its own KV-cache pool up front and lets nothing else allocate, a
+// plugin inside a framework that owns every allocation, and latency-bound
 // paths where cudaMalloc's implicit device synchronisation is not acceptable.
 // For them the scheduling counter of the dynamic work split lives here: a
 // file-scope device array that every GPU which loads this library holds until
@@ -2431,6 +2524,16 @@ int pmg_gather_noalloc(const void* cache, int64_t cache_block_stride, int64_t ca
   return launch_gather(pl, s);
 }
 
+
+int pmg_debug_noalloc_scratch(void** device_ptr, int64_t* num_ints) {
+  if (device_ptr == nullptr || num_ints == nullptr) return PMG_ERR_NULL;
+  int32_t* scratch = nullptr;
+  const int st = noalloc_scratch(&scratch);
+  if (st != PMG_OK) return st;
+  *device_ptr = scratch;
+  *num_ints = kNoAllocScratchInts;
+  return PMG_OK;
+}
 
 int pmg_gather_ex(const void* cache, int64_t cache_block_stride, int64_t cache_token_stride, int64_t num_blocks,
                   const int32_t* block_table, int64_t block_table_stride, const int32_t* cu_seq_lens,

@@ -210,6 +210,14 @@ def skew64(mode: str = "raw", seed: int = SEED_BASE + 4) -> Workload:
     raise ValueError(mode)
 
 
+def fp32_1m(seed: int = SEED_BASE + 6) -> Workload:
+    """1 request of 1,000,000 tokens of 576 fp32 elements (2304 bytes per
+    entry), raw copy, B=64, 16384 shuffled blocks: the output passes 2^31 bytes
+    after about 932K rows, where the review section ("评论区精华") of the page
+    reports int32 overflow of output_token_begin * entry_bytes."""
+    return make_workload("fp32-1M raw gather", [1_000_000], None, 64, 576, 16384, "fp32", "fp32", 1.0, seed)
+
+
 def p1test(cache_dtype: str = "bf16", use_seq_starts: bool = True, seed: int = SEED_BASE + 5) -> Workload:
     """The page's uneven test: lens {17, 32768, 71}, starts {3, 17, 5}, 1024
     blocks, every table row an independent permutation of all blocks.
@@ -226,4 +234,5 @@ CONFIGS: Dict[str, object] = {
     "skew8": skew8,
     "skew64_raw": lambda: skew64("raw"),
     "skew64_dequant": lambda: skew64("dequant"),
+    "fp32_1m": fp32_1m,
 }

@@ -22,8 +22,9 @@ def declared_functions():
 
 
 def test_header_declares_the_abi():
-    assert declared_functions() == ["pmg_debug_plan", "pmg_gather", "pmg_gather_ex", "pmg_gather_noalloc",
-                                    "pmg_gather_tokens", "pmg_select_path", "pmg_status_string", "pmg_version"]
+    assert declared_functions() == ["pmg_debug_noalloc_scratch", "pmg_debug_plan", "pmg_gather", "pmg_gather_ex",
+                                    "pmg_gather_noalloc", "pmg_gather_tokens", "pmg_select_path",
+                                    "pmg_status_string", "pmg_version"]
 
 
 def test_library_exports_every_declared_symbol(cuda_lib):

@@ -452,3 +452,34 @@ def test_cp_workspace_slice_eager_and_graph(name):
     g.replay()
     g.replay()
     check()
+
+
+# --- the exported pmg_gather symbol itself (no workspace, no options) ---------
+
+@pytest.mark.parametrize("name", ["tiny", "skew8", "skew64_dequant"])
+def test_pmg_gather_symbol_through_ctypes(name):
+    """pmg_gather, the call of ops.cp_gather_cache(src_cache, dst, block_table,
+    cu_seq_lens, batch_size, seq_starts) in section "关键源码片段" with strides,
+    dtypes, scale and stream made explicit, called directly through ctypes
+    with raw pointers, against the oracle."""
+    wl = W.CONFIGS[name]()
+    want, oflag = oracle_run(wl)
+    case = DeviceCase(wl)
+    L = binding.load_library()
+    codes = binding.DTYPE_CODES
+    st = L.pmg_gather(
+        case.cache.data_ptr(), case.cache.stride(0), case.cache.stride(1), case.cache.shape[0],
+        case.block_table.data_ptr(), case.block_table.shape[1], case.cu.data_ptr(),
+        None if case.seq_starts is None else case.seq_starts.data_ptr(), wl.num_reqs, case.T, wl.block_size,
+        wl.entry_size, codes[wl.src_dtype], codes[wl.dst_dtype], case.scale.data_ptr(), case.dst.data_ptr(),
+        case.dst.stride(0), case.err.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert st == 0, binding.status_string(st)
+    got, flag, guards = case.result()
+    assert guards and flag == oflag == 0
+    assert_same(got, want, wl.dst_dtype, wl.src_dtype != wl.dst_dtype)
+
+
+def test_fp32_1m_named_workload_with_workspace():
+    """The 1M-token fp32 raw copy the benchmark times (2304-byte entries, output
+    offsets past 2^31 bytes), in the benchmark's launch configuration."""
+    _check(W.CONFIGS["fp32_1m"](), workspace=True)

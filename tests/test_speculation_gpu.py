@@ -200,3 +200,58 @@ def test_many_requests_metadata_race(R, with_ss, implied):
         got = out.cpu().view(torch.int16).numpy().view(np.uint16)
         assert int(err.item()) == flag == 0
         assert_same(got, want, "bf16", False)
+
+
+@pytest.mark.parametrize("src,dst", [("bf16", "bf16"), ("fp8_e4m3", "bf16")])
+@pytest.mark.parametrize("form", ["zero_to_T", "offset_start", "short_end", "implied_zero", "implied_offset"])
+def test_single_request_plan_guess_under_race(src, dst, form):
+    """One request without seq_starts: the TMA paths plan from cu_seq_lens =
+    [0, T] (or [0] with the implied end) before reading it, and keep that plan
+    only if the values read after the previous grid completes agree. Here the
+    previous grid writes the next call's cu_seq_lens and block table; forms
+    that differ from the guess (a start above 0, an end below T) must give the
+    oracle's result on the new tables, bit for bit."""
+    dev = "cuda:0"
+    E, STRIDE1 = 64, 24
+    rng = np.random.default_rng({"zero_to_T": 81, "offset_start": 82, "short_end": 83, "implied_zero": 84,
+                                 "implied_offset": 85}[form] + (100 if src != dst else 0))
+    wl = W.make_workload("spec1", [B * NB], None, B, E, NB, src, dst, 0.05, 86)
+    cache = wl.cache.to(dev)
+    cache_bits = W.tensor_bits(wl.cache)
+    scale = torch.tensor([wl.scale], dtype=torch.float32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    one_bt = torch.zeros(1, 1, dtype=torch.int32, device=dev)
+    one_cu = torch.tensor([0, 1], dtype=torch.int32, device=dev)
+    implied = form.startswith("implied")
+    opts = binding.OPT_IMPLIED_END if implied else 0
+    meta = torch.empty(64, dtype=torch.int32, device=dev)
+    for it in range(16):
+        T = int(rng.integers(B, STRIDE1 * B))
+        c0 = int(rng.integers(1, B)) if form in ("offset_start", "implied_offset") else 0
+        c1 = int(rng.integers(c0 + 1, T)) if form == "short_end" else T
+        new = np.zeros(64, np.int32)
+        new[0], new[1] = c0, (0 if implied else c1)
+        new[16:16 + STRIDE1] = rng.permutation(NB)[:STRIDE1]
+        old = np.zeros(64, np.int32)
+        old[0], old[1] = 0, (0 if implied else T)  # the form the guess assumes
+        old[16:16 + STRIDE1] = rng.permutation(NB)[:STRIDE1]
+        src_row = torch.from_numpy(new.view(np.float32).copy()).to(dev).view(1, 1, 64)
+        meta.copy_(torch.from_numpy(old))
+        out = torch.empty((T, E), dtype=W.TORCH_DTYPES[dst], device=dev)
+        out.view(torch.uint8).fill_(0xA5)
+        err.zero_()
+        torch.cuda.synchronize()
+        torch.cuda._sleep(200_000)
+        binding.gather(src_row, meta.view(torch.float32).view(1, 64), one_bt, one_cu, error_flag=err)
+        binding.gather(cache, out, meta[16:16 + STRIDE1].view(1, STRIDE1), meta[:1 if implied else 2], None, scale,
+                       err, num_reqs=1, options=opts)
+        torch.cuda.synchronize()
+        assert np.array_equal(meta.cpu().numpy(), new)
+        cu = np.array([c0, T if implied else c1], np.int32)
+        ed = W.ELEM_BYTES[dst]
+        want = np.full((T, E * ed), 0xA5, np.uint8).view(W.NP_BITS[ed])
+        flag = og.gather(cache_bits, new[16:16 + STRIDE1].reshape(1, STRIDE1).copy(), cu, None, 1, T, B, E, src,
+                         dst, wl.scale, want)
+        got = out.cpu().view(torch.uint8).numpy().view(W.NP_BITS[ed]).reshape(T, E)
+        assert int(err.item()) == flag == 0
+        assert_same(got, want, dst, src != dst)
