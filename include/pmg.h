@@ -69,15 +69,16 @@ typedef enum pmg_status {
 #define PMG_FLAG_LOGICAL_BLOCK 1 /* logical block >= block_table_stride: page skipped */
 #define PMG_FLAG_PHYS_BLOCK 2    /* block_table entry outside [0, num_blocks): page skipped */
 #define PMG_FLAG_SEQ_START 4     /* seq_starts[r] < 0 with len_r > 0: request skipped */
-#define PMG_FLAG_CU_ORDER 8      /* cu_seq_lens[0] < 0 or cu decreases: nothing written */
+#define PMG_FLAG_CU_ORDER 8      /* a request's rows start below row 0 or an earlier cu boundary: request skipped */
 #define PMG_FLAG_TIMEOUT 16      /* a bounded device wait ran out: output incomplete */
 #define PMG_FLAG_TOKEN 32        /* pmg_gather_tokens: request id or row range of a token invalid: token skipped */
 
 /* Requests one launch plans in shared memory. A call with more requests needs
- * a workspace (pmg_gather_ex, or pmg_gather_noalloc) and runs as a validation
- * of the whole cu_seq_lens, one launch per group of PMG_MAX_REQS_PLAN
- * requests, and a final one-thread launch; without a workspace it returns
- * PMG_ERR_UNSUPPORTED. pmg_debug_plan is limited to this many. */
+ * a workspace (pmg_gather_ex, or pmg_gather_noalloc) and runs as one launch
+ * per group of PMG_MAX_REQS_PLAN requests (each group passes the highest
+ * cu_seq_lens boundary so far to the next through the workspace) and a final
+ * one-thread launch; without a workspace it returns PMG_ERR_UNSUPPORTED.
+ * pmg_debug_plan is limited to this many. */
 #define PMG_MAX_REQS_PLAN 4096
 
 /* Most requests one call accepts; more return PMG_ERR_UNSUPPORTED. */
@@ -119,8 +120,12 @@ typedef enum pmg_path {
  *                      (i+1)*block_size) of its context) to a physical block.
  *  cu_seq_lens         int32 [num_reqs + 1]: request r owns output rows
  *                      [min(cu[r], T), min(cu[r+1], T)); its length is
- *                      max(min(cu[r+1], T) - min(cu[r], T), 0). Must be
- *                      non-decreasing from cu[0] >= 0 (else PMG_FLAG_CU_ORDER).
+ *                      max(min(cu[r+1], T) - min(cu[r], T), 0), so a decrease
+ *                      only gives a request no rows. A request with rows whose
+ *                      first row min(cu[r], T) is below 0 or below an earlier
+ *                      boundary min(cu[j], T), j < r (its rows would overlap
+ *                      earlier rows or come out of order) is skipped and
+ *                      PMG_FLAG_CU_ORDER is set; the other requests are copied.
  *  seq_starts          int32 [num_reqs] or NULL (all zero): the first context
  *                      token of request r to copy.
  *  num_reqs            0 <= num_reqs <= PMG_MAX_REQS_PLAN (pmg_gather) or
@@ -283,8 +288,9 @@ int pmg_select_path(const void* cache, int64_t cache_block_stride, int64_t cache
  *                 output_token_begin} for t < min(num_tasks, max_tasks).
  *  num_tasks_out  device int64 scalar: the number of tasks.
  *  error_flag     as in pmg_gather (PMG_FLAG_SEQ_START, PMG_FLAG_CU_ORDER).
- * A request with len 0 or a negative start has no task; an invalid
- * cu_seq_lens gives 0 tasks. The block table is not read.
+ * A request with len 0, a negative start, or rows starting below an earlier
+ * cu_seq_lens boundary (PMG_FLAG_CU_ORDER) has no task. The block table is
+ * not read.
  */
 int pmg_debug_plan(const int32_t* cu_seq_lens, const int32_t* seq_starts, int32_t num_reqs, int64_t total_tokens,
                    int32_t block_size, int32_t* tasks_out, int64_t max_tasks, int64_t* num_tasks_out,

@@ -20,8 +20,10 @@ Readings where the page leaves a case open:
 - len == 0 gives no page. (The page's formula yields one empty page when
   start is not a multiple of B; it copies nothing, so outputs are the same.)
 - A request with len > 0 and a negative start gives no page.
-- cu_seq_lens that decreases anywhere, or a negative cu[0], gives no task at
-  all (the caller gets a flag instead).
+- A request with len > 0 whose output_begin is below an earlier boundary of
+  cu_seq_lens (some min(cu[j], T), j < r) or below row 0 gives no page: its
+  rows would overlap earlier rows or run out of order (the caller gets a
+  flag). A decrease of cu_seq_lens by itself only gives len == 0.
 """
 from __future__ import annotations
 
@@ -38,17 +40,16 @@ def _request_span(cu: Sequence[int], seq_starts: Optional[Sequence[int]], r: int
     return ob, length, start
 
 
-def cu_is_valid(cu: Sequence[int], num_reqs: int) -> bool:
-    if num_reqs == 0:
-        return True
-    if int(cu[0]) < 0:
-        return False
-    return all(int(cu[r + 1]) >= int(cu[r]) for r in range(num_reqs))
+def below_earlier_boundary(cu: Sequence[int], r: int, T: int) -> bool:
+    """Whether request r's first output row lies below row 0 or below
+    min(cu[j], T) for some j < r."""
+    ob = min(int(cu[r]), T)
+    return ob < max([0] + [min(int(cu[j]), T) for j in range(r)])
 
 
 def pages_of_request(cu, seq_starts, r: int, T: int, B: int) -> int:
     ob, length, start = _request_span(cu, seq_starts, r, T)
-    if length == 0 or start < 0:
+    if length == 0 or start < 0 or below_earlier_boundary(cu, r, T):
         return 0
     first = start // B
     last_exclusive = -(-(start + length) // B)  # ceil
@@ -58,13 +59,11 @@ def pages_of_request(cu, seq_starts, r: int, T: int, B: int) -> int:
 def page_tasks(cu: Sequence[int], seq_starts: Optional[Sequence[int]], num_reqs: int,
                total_tokens: int, block_size: int) -> List[Task]:
     """All tasks, in task-id order, by walking each request's logical pages."""
-    if not cu_is_valid(cu, num_reqs):
-        return []
     B, T = block_size, total_tokens
     tasks: List[Task] = []
     for r in range(num_reqs):
         ob, length, start = _request_span(cu, seq_starts, r, T)
-        if length == 0 or start < 0:
+        if length == 0 or start < 0 or below_earlier_boundary(cu, r, T):
             continue
         lb = start // B
         while lb * B < start + length:
@@ -82,8 +81,6 @@ def task_by_scan(task_id: int, cu: Sequence[int], seq_starts: Optional[Sequence[
     """One task from its flat id the way the page's mapper finds it: walk the
     requests in order, take away each request's page count from the id until
     the id falls inside a request. Returns None past the last task."""
-    if not cu_is_valid(cu, num_reqs):
-        return None
     B, T = block_size, total_tokens
     rel = task_id
     for r in range(num_reqs):
@@ -100,6 +97,4 @@ def task_by_scan(task_id: int, cu: Sequence[int], seq_starts: Optional[Sequence[
 
 
 def num_tasks(cu, seq_starts, num_reqs: int, total_tokens: int, block_size: int) -> int:
-    if not cu_is_valid(cu, num_reqs):
-        return 0
     return sum(pages_of_request(cu, seq_starts, r, total_tokens, block_size) for r in range(num_reqs))

@@ -19,10 +19,13 @@
  * its source starts at seq_starts[r] (0 when seq_starts is absent).
  *
  * Readings where the page is silent:
- *  - cu_seq_lens must be non-decreasing from a non-negative cu[0]; otherwise
- *    the output rows of two requests could overlap and the result would
- *    depend on the order of writes. Such a call writes nothing and reports
- *    bit 8.
+ *  - The page's clamp decides each request's rows: a decrease of cu_seq_lens
+ *    gives the request there no rows, and the other requests are copied as
+ *    usual. What the page leaves open is a request with rows whose first row
+ *    lies below an earlier boundary of cu_seq_lens (below cu[j] for some
+ *    j < r, or below row 0): its rows would overlap rows written before, in
+ *    an order the page does not fix, or run out of order. Such a request is
+ *    skipped (bit 8); every other request is still copied.
  *  - A request with len > 0 and a negative start writes nothing (bit 4).
  *  - A token whose logical block is >= block_table_stride (bit 1) or whose
  *    physical block id is outside [0, num_blocks) (bit 2) is skipped; its
@@ -204,17 +207,19 @@ int pmg_oracle_gather(const uint8_t* cache, int64_t cache_block_stride, int64_t 
   const int64_t B = block_size;
   int flag = 0;
 
-  if (num_reqs > 0) {
-    if (cu_seq_lens[0] < 0) return O_BAD_CU;
-    for (int32_t r = 0; r < num_reqs; ++r)
-      if (cu_seq_lens[r + 1] < cu_seq_lens[r]) return O_BAD_CU;
-  }
-
+  /* the highest of row 0 and the clamped boundaries cu[0..r-1] */
+  int64_t floor_row = 0;
   for (int32_t r = 0; r < num_reqs; ++r) {
     const int64_t ob = cu_seq_lens[r] < T ? cu_seq_lens[r] : T;
     const int64_t oe = cu_seq_lens[r + 1] < T ? cu_seq_lens[r + 1] : T;
     const int64_t len = oe - ob > 0 ? oe - ob : 0;
     const int64_t start = seq_starts ? (int64_t)seq_starts[r] : 0;
+    const int64_t below = floor_row;
+    if (ob > floor_row) floor_row = ob;
+    if (len > 0 && ob < below) {
+      flag |= O_BAD_CU;
+      continue;
+    }
     if (len > 0 && start < 0) {
       flag |= O_BAD_START;
       continue;

@@ -102,7 +102,8 @@ struct Params {
   const float* scale;     // may be null
   int32_t* err;           // may be null
   int32_t* sched;         // work-claim counter in the caller's workspace, or null (static split)
-  const int32_t* gate;    // large batches: non-zero when cu_seq_lens failed validation (write nothing)
+  const int32_t* carry_in;  // large batches: highest cu_seq_lens boundary of the groups before (or null)
+  int32_t* carry_out;       // large batches: where this group's highest boundary goes for the next group
   int32_t early;          // plan and first block ids before the previous grid completes (caller's promise)
   int32_t spec;           // plan and first batch before the previous grid completes, checked after it
   int32_t spec_guess;     // speculative start of one request without seq_starts: assume cu = [0, T]
@@ -226,12 +227,60 @@ __device__ __forceinline__ int32_t request_pages(const PlanView& v, int r, int B
 }
 
 // Builds the plan. kWarp = false: all threads of the CTA take part (any R up
-// to PMG_MAX_REQS_PLAN). kWarp = true: one warp builds it alone, with no CTA-wide
-// barrier, for R <= kWarpPlanMaxReqs. Returns the number of page tasks, or -1
-// when cu_seq_lens is not non-decreasing from a non-negative start (then
-// nothing may be written). report_flags: this CTA reports the plan-level flag
-// bits (one CTA per launch does, to keep atomics rare).
+// to PMG_MAX_REQS_PLAN). kWarp = true: one warp builds it alone, with no
+// CTA-wide barrier, for R <= kWarpPlanMaxReqs. Returns the number of page
+// tasks. report_flags: this CTA reports the plan-level flag bits (one CTA per
+// launch does, to keep atomics rare) and, for a group of a large batch, passes
+// the highest boundary on to the next group.
+//
+// Output placement is the page's clamp: request r owns rows [c_r, c_{r+1})
+// with c_r = min(cu[r], T) when c_{r+1} > c_r, and none otherwise. A request
+// with rows whose first row lies below row 0 or below an earlier boundary
+// (c_r < m_r, m_r = max(0, c_0, ..., c_r), the highest boundary so far) would
+// overlap rows written before it, or run out of order: it is skipped
+// (PMG_FLAG_CU_ORDER) and every other request is copied. The plan keeps
+// ob[r] = m_r, which never decreases, so a binary search finds the request of
+// any output row: a copied request has m_r = c_r and m_{r+1} = c_{r+1}; a
+// request without rows has m_{r+1} = m_r; a skipped request keeps the rows
+// [m_r, m_{r+1}) to itself (they stay untouched) and has kSkipStart as its
+// start, so it has no pages.
 constexpr int kWarpPlanMaxReqs = 256;
+constexpr int32_t kSkipStart = INT32_MIN;
+
+// Exclusive scan with max over the threads' values, in thread order; the
+// first thread gets `init`.
+template <bool kWarp>
+__device__ __forceinline__ int32_t exclusive_max_scan(int32_t x, int32_t init, int32_t* warp_vals) {
+  const int tid = kWarp ? static_cast<int>(threadIdx.x & 31) : static_cast<int>(threadIdx.x);
+  const int lane = tid & 31;
+  int32_t inc = x;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t y = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc = max(inc, y);
+  }
+  int32_t exc = __shfl_up_sync(0xffffffffu, inc, 1);
+  exc = lane == 0 ? init : max(exc, init);
+  if constexpr (!kWarp) {
+    const int warp = tid >> 5;
+    const int nwarps = (static_cast<int>(blockDim.x) + 31) >> 5;
+    if (lane == 31) warp_vals[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+      int32_t w = lane < nwarps ? warp_vals[lane] : INT32_MIN;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int32_t y = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w = max(w, y);
+      }
+      if (lane < nwarps) warp_vals[lane] = w;
+    }
+    __syncthreads();
+    if (warp > 0) exc = max(exc, warp_vals[warp - 1]);
+    __syncthreads();
+  }
+  return exc;
+}
 
 template <bool kWarp>
 __device__ int build_plan(const Params& p, const PlanView& v, bool report_flags, int* flags_out = nullptr,
@@ -243,61 +292,100 @@ __device__ int build_plan(const Params& p, const PlanView& v, bool report_flags,
   const int R = p.R;
   const int64_t T = p.T;
 
-  int bad = 0;
-  int bad_start = 0;
+  int bad_cu = 0, bad_start = 0;
   const uint64_t keep = evict_last_policy();
+  const int32_t carry = (p.carry_in != nullptr) ? ld_meta(p.carry_in, keep) : 0;
   if constexpr (kWarp) {
-    // every CTA reads these few lines at once: one load per entry, and
-    // cu[r - 1] comes from the neighbouring lane (or the previous pass)
-    int64_t carry = 0;
+    // One pass per 32 boundaries, in registers: lane l holds c_r (r = base +
+    // l) and m_r; request r - 1 is decided from c_{r-1} and m_{r-1} of the
+    // lane before (or of the previous pass).
+    int32_t prev_c = 0, prev_m = max(carry, 0), prev_s = 0;
     for (int base = 0; base <= R; base += 32) {
       const int r = base + tid;
-      const bool implied = p.implied_end && r == R;
+      const bool implied = p.implied_end && r == R;  // the last request ends at T
       const int32_t cur32 = (r <= R && !implied) ? ld_meta(p.cu + r, keep) : 0;
       const int32_t start = (r < R && p.ss != nullptr) ? ld_meta(p.ss + r, keep) : 0;
       if (raw_cu != nullptr && r <= R) raw_cu[r] = cur32;
-      const int64_t cur = cur32;
-      const int64_t up = __shfl_up_sync(0xffffffffu, cur, 1);
-      const int64_t prev = tid == 0 ? carry : up;
-      carry = __shfl_sync(0xffffffffu, cur, 31);
-      if (r <= R) {
-        const int64_t c = implied ? (prev > T ? prev : T) : cur;
-        if (r == 0 && c < 0) bad = 1;
-        if (r > 0 && !implied && c < prev) bad = 1;
-        v.ob[r] = static_cast<int32_t>(c < T ? c : T);
-        if (r < R) v.st[r] = start;
+      const int64_t c64 = implied ? T : static_cast<int64_t>(cur32);
+      const int32_t c = r <= R ? static_cast<int32_t>(c64 < T ? c64 : T) : INT32_MIN;
+      int32_t m = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int32_t y = __shfl_up_sync(0xffffffffu, m, o);
+        if (tid >= o) m = max(m, y);
       }
+      m = max(m, prev_m);
+      const int32_t up_c = __shfl_up_sync(0xffffffffu, c, 1);
+      const int32_t up_m = __shfl_up_sync(0xffffffffu, m, 1);
+      const int32_t up_s = __shfl_up_sync(0xffffffffu, start, 1);
+      const int32_t c_prev = tid == 0 ? prev_c : up_c;
+      const int32_t m_prev = tid == 0 ? prev_m : up_m;
+      const int32_t s_prev = tid == 0 ? prev_s : up_s;
+      if (r >= 1 && r <= R) {
+        // request r - 1 owns [c_prev, c) under the page's clamp
+        const bool has_rows = c > c_prev;
+        const bool skip = has_rows && c_prev < m_prev;
+        bad_cu |= skip ? 1 : 0;
+        bad_start |= (has_rows && !skip && s_prev < 0) ? 1 : 0;
+        v.st[r - 1] = skip ? kSkipStart : s_prev;
+      }
+      if (r <= R) v.ob[r] = m;
+      prev_c = __shfl_sync(0xffffffffu, c, 31);
+      prev_m = __shfl_sync(0xffffffffu, m, 31);
+      prev_s = __shfl_sync(0xffffffffu, start, 31);
     }
+    __syncwarp();
   } else {
+    // 1. the clamped boundaries c_r into ob and the starts into st; the loads
+    // of an entry are issued together
     for (int r = tid; r <= R; r += nt) {
-      // the three loads first, so that they share one round trip
-      const bool implied = p.implied_end && r == R;
-      const int64_t cur = implied ? 0 : static_cast<int64_t>(ld_meta(p.cu + r, keep));
-      const int64_t prev = r > 0 ? static_cast<int64_t>(ld_meta(p.cu + r - 1, keep)) : 0;
+      const bool implied = p.implied_end && r == R;  // the last request ends at T
+      const int32_t cur32 = implied ? 0 : ld_meta(p.cu + r, keep);
       const int32_t start = (r < R && p.ss != nullptr) ? ld_meta(p.ss + r, keep) : 0;
-      const int64_t c = implied ? (prev > T ? prev : T) : cur;
-      if (r == 0 && c < 0) bad = 1;
-      if (r > 0 && !implied && c < prev) bad = 1;
+      if (raw_cu != nullptr) raw_cu[r] = cur32;
+      const int64_t c = implied ? T : static_cast<int64_t>(cur32);
       v.ob[r] = static_cast<int32_t>(c < T ? c : T);
       if (r < R) v.st[r] = start;
     }
+    __syncthreads();
+    // 2. m_r = max(0, carried boundary, c_0..c_r) into P (scratch for now);
+    // each thread owns a contiguous run of boundaries
+    const int nb = R + 1;
+    const int per_b = (nb + nt - 1) / nt;
+    const int bb = min(tid * per_b, nb);
+    const int be = min(bb + per_b, nb);
+    int32_t run_max = INT32_MIN;
+    for (int r = bb; r < be; ++r) run_max = max(run_max, v.ob[r]);
+    int32_t m = exclusive_max_scan<false>(run_max, max(carry, 0), warp_sums);
+    for (int r = bb; r < be; ++r) {
+      m = max(m, v.ob[r]);
+      v.P[r] = m;
+    }
+    __syncthreads();
+    // 3. per request: skip the ones with rows below an earlier boundary; flag
+    // negative starts of the others
+    for (int r = tid; r < R; r += nt) {
+      const int32_t c = v.ob[r];
+      const bool has_rows = v.ob[r + 1] > c;
+      if (has_rows && c < v.P[r]) {
+        bad_cu = 1;
+        v.st[r] = kSkipStart;
+      } else if (has_rows && v.st[r] < 0) {
+        bad_start = 1;
+      }
+    }
+    __syncthreads();
+    for (int r = bb; r < be; ++r) v.ob[r] = v.P[r];
+    __syncthreads();
   }
-  const bool any_bad = kWarp ? (__syncwarp(), __any_sync(0xffffffffu, bad)) : __syncthreads_or(bad);
-  if (any_bad) {
-    if (report_flags && tid == 0) set_flag(p, PMG_FLAG_CU_ORDER);
-    if (flags_out != nullptr) *flags_out = PMG_FLAG_CU_ORDER;
-    return -1;
-  }
-
-  // exclusive scan of page counts: each thread owns a contiguous run of requests
+  if (report_flags && tid == 0 && p.carry_out != nullptr) *p.carry_out = v.ob[R];
   const int per = (R + nt - 1) / nt;
   const int rb = min(tid * per, R);
   const int re = min(rb + per, R);
+
+  // exclusive scan of page counts: each thread owns a contiguous run of requests
   int32_t local = 0;
-  for (int r = rb; r < re; ++r) {
-    local += request_pages(v, r, p.B);
-    if (v.st[r] < 0 && v.ob[r + 1] > v.ob[r]) bad_start = 1;
-  }
+  for (int r = rb; r < re; ++r) local += request_pages(v, r, p.B);
   const int lane = tid & 31;
   int32_t x = local;
 #pragma unroll
@@ -333,9 +421,16 @@ __device__ int build_plan(const Params& p, const PlanView& v, bool report_flags,
     base += request_pages(v, r, p.B);
   }
   if (tid == 0) v.P[R] = total;
-  const bool any_bad_start = kWarp ? (__syncwarp(), __any_sync(0xffffffffu, bad_start)) : __syncthreads_or(bad_start);
-  if (any_bad_start && report_flags && tid == 0) set_flag(p, PMG_FLAG_SEQ_START);
-  if (flags_out != nullptr) *flags_out = any_bad_start ? PMG_FLAG_SEQ_START : 0;
+  int flags = 0;
+  if (kWarp) {
+    __syncwarp();
+    flags = (__any_sync(0xffffffffu, bad_cu) ? PMG_FLAG_CU_ORDER : 0) |
+            (__any_sync(0xffffffffu, bad_start) ? PMG_FLAG_SEQ_START : 0);
+  } else {
+    flags = (__syncthreads_or(bad_cu) ? PMG_FLAG_CU_ORDER : 0) | (__syncthreads_or(bad_start) ? PMG_FLAG_SEQ_START : 0);
+  }
+  if (report_flags && tid == 0) set_flag(p, flags);
+  if (flags_out != nullptr) *flags_out = flags;
   return total;
 }
 
@@ -1289,7 +1384,6 @@ __global__ void __launch_bounds__(kBulkThreads) gather_bulk_kernel(const __grid_
   // cache, scale or workspace and every write of dst comes after the wait.
   const bool early = p.early != 0 || p.spec != 0;
   if (!early) pdl_wait();
-  if (p.gate != nullptr && *reinterpret_cast<const volatile int32_t*>(p.gate) != 0) return;
   __syncthreads();
   // small batches: the scheduler warp plans alone; large ones: the whole CTA;
   // the per-token gather needs no plan
@@ -1526,7 +1620,6 @@ __global__ void __launch_bounds__(kPlanThreads) gather_simt_kernel(const __grid_
   const PlanView v = plan_view(smem, p);
   prefetch_metadata(p);
   pdl_entry();
-  if (p.gate != nullptr && *reinterpret_cast<const volatile int32_t*>(p.gate) != 0) return;
   const int32_t num_tasks = build_plan<false>(p, v, blockIdx.x == 0);
   if (num_tasks <= 0) return;
   const CtaRange range = cta_range(v, p.R, p.B, num_tasks);
@@ -1666,7 +1759,6 @@ __global__ void __launch_bounds__(kCvtThreads) gather_tma_convert_kernel(const _
   // cache, scale or workspace and every write of dst comes after the wait.
   const bool early = p.early != 0 || p.spec != 0;
   if (!early) pdl_wait();
-  if (p.gate != nullptr && *reinterpret_cast<const volatile int32_t*>(p.gate) != 0) return;
   __syncthreads();
   // small batches: the scheduler warp plans alone; large ones: the whole CTA;
   // the per-token gather needs no plan
@@ -1880,31 +1972,19 @@ __global__ void __launch_bounds__(kTokThreads) gather_tokens_kernel(const __grid
 
 // ---------------------------------------------------------------------------
 // Large batches (more requests than one launch plans in shared memory) run as
-// consecutive launches over groups of requests. cu_seq_lens is validated as a
-// whole first, so that an invalid array still writes nothing at all; the
-// verdict lives in the caller's workspace and is cleared by the last step.
+// consecutive launches over groups of requests. A group's plan needs the
+// highest cu_seq_lens boundary of the groups before it (a request is skipped
+// when its rows start below it): each group's first CTA leaves that value in
+// one of two workspace slots for the next group, which reads it only after the
+// group before has completed; a final one-thread launch clears the slots.
 // ---------------------------------------------------------------------------
 
-__global__ void __launch_bounds__(1024) validate_cu_kernel(const int32_t* cu, int32_t R, int32_t T, int32_t implied_end,
-                                                          int32_t* gate, int32_t* err) {
-  pdl_entry();
-  int bad = 0;
-  const int64_t n = implied_end ? R : static_cast<int64_t>(R) + 1;
-  for (int64_t r = threadIdx.x; r < n; r += blockDim.x) {
-    const int32_t c = cu[r];
-    if (r == 0 && c < 0) bad = 1;
-    if (r > 0 && c < cu[r - 1]) bad = 1;
-  }
-  (void)T;
-  if (__syncthreads_or(bad) && threadIdx.x == 0) {
-    *gate = 1;
-    if (err != nullptr) atomicOr(err, PMG_FLAG_CU_ORDER);
-  }
-}
+constexpr int kCarrySlot = 2;  // workspace ints 2 and 3
+static_assert(kCarrySlot + 2 <= PMG_WORKSPACE_INTS, "the carried boundaries must fit the workspace");
 
-__global__ void clear_gate_kernel(int32_t* gate) {
+__global__ void clear_carry_kernel(int32_t* ws) {
   pdl_entry();
-  if (threadIdx.x == 0) *gate = 0;
+  if (threadIdx.x < 2) ws[kCarrySlot + threadIdx.x] = 0;
 }
 
 // ---------------------------------------------------------------------------
@@ -2105,8 +2185,8 @@ int make_plan(const void* cache, int64_t cbs, int64_t cts, int64_t num_blocks, c
   if (options & ~(PMG_OPT_FORCE_SIMT | PMG_OPT_FORCE_SCALAR | PMG_OPT_IMPLIED_END | PMG_OPT_EARLY_METADATA))
     return PMG_ERR_ARG;
   if (R > PMG_MAX_REQS) return PMG_ERR_UNSUPPORTED;
-  // more requests than one launch plans need the workspace (for the verdict
-  // of the whole-array validation)
+  // more requests than one launch plans need the workspace (it carries the
+  // highest cu_seq_lens boundary from one group of requests to the next)
   if (R > PMG_MAX_REQS_PLAN && workspace == nullptr) return PMG_ERR_UNSUPPORTED;
   const int es = elem_bytes(sdt), ed = elem_bytes(ddt);
   if (static_cast<int64_t>(E) * ed > INT32_MAX || static_cast<int64_t>(E) * es > INT32_MAX) return PMG_ERR_UNSUPPORTED;
@@ -2402,32 +2482,21 @@ int launch_one(const Plan& pl, cudaStream_t stream) {
   return cudaGetLastError() == cudaSuccess ? PMG_OK : PMG_ERR_CUDA;
 }
 
-// One call: a single launch, or, beyond PMG_MAX_REQS_PLAN requests, the
-// whole-array validation, one launch per group of requests (pointers into
-// cu_seq_lens, seq_starts and the block table advance by the group; output
-// rows come from the absolute cu values, so every group writes its own rows),
-// and the clearing of the verdict.
+// One call: a single launch, or, beyond PMG_MAX_REQS_PLAN requests, one launch
+// per group of requests (pointers into cu_seq_lens, seq_starts and the block
+// table advance by the group; output rows come from the absolute cu values,
+// so every group writes its own rows; group g reads the highest boundary so
+// far from workspace slot (g - 1) % 2 and writes its own to slot g % 2), and
+// the clearing of the two slots.
 int launch_gather(const Plan& pl, cudaStream_t stream) {
   const Params& q = pl.prm;
   if (q.R <= PMG_MAX_REQS_PLAN) return launch_one(pl, stream);
   int sms = 0;
   int st = device_setup(&sms);
   if (st != PMG_OK) return st;
-  int32_t* gate = q.sched + 1;
-  {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(1);
-    cfg.blockDim = dim3(1024);
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = use_pdl() ? 1 : 0;
-    if (cudaLaunchKernelEx(&cfg, validate_cu_kernel, q.cu, q.R, q.T, q.implied_end, gate, q.err) != cudaSuccess)
-      return PMG_ERR_CUDA;
-  }
-  for (int64_t r0 = 0; r0 < q.R; r0 += PMG_MAX_REQS_PLAN) {
+  int32_t* slots = q.sched + kCarrySlot;
+  int64_t g_index = 0;
+  for (int64_t r0 = 0; r0 < q.R; r0 += PMG_MAX_REQS_PLAN, ++g_index) {
     Plan g = pl;
     const int32_t rg = static_cast<int32_t>(std::min<int64_t>(PMG_MAX_REQS_PLAN, q.R - r0));
     g.prm.R = rg;
@@ -2435,7 +2504,8 @@ int launch_gather(const Plan& pl, cudaStream_t stream) {
     g.prm.ss = q.ss ? q.ss + r0 : nullptr;
     g.prm.bt = q.bt + r0 * q.bt_stride;
     g.prm.implied_end = (q.implied_end && r0 + rg == q.R) ? 1 : 0;
-    g.prm.gate = gate;
+    g.prm.carry_in = g_index == 0 ? nullptr : slots + ((g_index - 1) & 1);
+    g.prm.carry_out = slots + (g_index & 1);
     st = launch_one(g, stream);
     if (st != PMG_OK) return st;
   }
@@ -2448,7 +2518,7 @@ int launch_gather(const Plan& pl, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = use_pdl() ? 1 : 0;
-  if (cudaLaunchKernelEx(&cfg, clear_gate_kernel, gate) != cudaSuccess) return PMG_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, clear_carry_kernel, q.sched) != cudaSuccess) return PMG_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? PMG_OK : PMG_ERR_CUDA;
 }
 

@@ -87,3 +87,32 @@ def test_random_gather_many_requests(seed):
     assert guards, "guard regions written"
     assert flag == oflag
     assert_same(got, want, wl.dst_dtype, wl.src_dtype != wl.dst_dtype)
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_random_gather_cu_not_non_decreasing(seed):
+    """cu_seq_lens with random decreases (and now and then a negative first
+    entry): requests after a decrease lose their rows or, when their rows would
+    start below an earlier boundary, are skipped with flag 8; everything else
+    is copied. Half the cases have more than 256 requests (the plan built by
+    the whole CTA), the rest fewer (the one-warp plan)."""
+    rng = np.random.default_rng(97_000 + seed)
+    if seed % 2:
+        wl, options, workspace = _case_many(seed + 100)
+    else:
+        wl, _, options, workspace = _case(seed + 500)
+    cu = wl.cu_seq_lens.numpy().astype(np.int64)
+    R = wl.num_reqs
+    for _ in range(int(rng.integers(1, 4))):
+        i = int(rng.integers(0, R + 1))
+        cu[i] = cu[i] - int(rng.integers(1, 40)) if rng.random() < 0.8 else cu[i] + int(rng.integers(1, 10))
+    if rng.random() < 0.2:
+        cu[0] = -int(rng.integers(1, 5))
+    cu = cu.astype(np.int32)
+    case = DeviceCase(wl, cu=cu, workspace=workspace)
+    case.run(options=options)
+    got, flag, guards = case.result()
+    want, oflag = oracle_run(wl, cu=cu)
+    assert guards, "guard regions written"
+    assert flag == oflag
+    assert_same(got, want, wl.dst_dtype, wl.src_dtype != wl.dst_dtype)

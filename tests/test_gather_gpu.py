@@ -265,10 +265,21 @@ def test_negative_seq_start():
     _check(wl, seq_starts=np.array([3, -5, 7], np.int32), expect_flag=og.BAD_START)
 
 
-@pytest.mark.parametrize("cu", [[0, 40, 30, 95], [-1, 40, 70, 95], [0, 40, 70, 60]])
-def test_invalid_cu_writes_nothing(cu):
+# cu_seq_lens that is not non-decreasing: the page's clamp gives a request
+# after a decrease no rows; a request whose rows would start below row 0 or
+# below an earlier boundary (overlapping or out-of-order rows) is skipped with
+# flag 8, and every other request is copied (T = 95, lengths 40/30/25)
+@pytest.mark.parametrize("cu,flag", [
+    ([0, 40, 30, 30], 0),             # a decrease, no rows after it
+    ([0, 40, 70, 60], 0),             # the last request has no rows
+    ([0, 40, 30, 95], og.BAD_CU),     # request 2 would overlap request 0
+    ([-1, 40, 70, 95], og.BAD_CU),    # request 0 would start at row -1
+    ([50, 60, 0, 20], og.BAD_CU),     # request 2 comes out of order (no overlap)
+    ([0, 40, 20, 60], og.BAD_CU),     # rows 40-59 of the skipped request stay untouched
+])
+def test_cu_seq_lens_not_non_decreasing(cu, flag):
     wl = _flag_case()
-    _check(wl, cu=np.array(cu, np.int32), expect_flag=og.BAD_CU)
+    _check(wl, cu=np.array(cu, np.int32), expect_flag=flag)
 
 
 def test_huge_seq_start_no_overflow():
@@ -276,7 +287,7 @@ def test_huge_seq_start_no_overflow():
     _check(wl, seq_starts=np.array([3, 2 ** 31 - 10, 7], np.int32), expect_flag=og.BAD_LOGICAL)
 
 
-# --- batches beyond one launch's plan: validated, then run in groups -----------
+# --- batches beyond one launch's plan: run in groups of requests -------------
 
 def _large(R, seed, src="bf16", dst="bf16", E=64, B=16):
     rng = np.random.default_rng(seed)
@@ -300,12 +311,19 @@ def test_large_batch_needs_a_workspace():
     assert e.value.status == 5
 
 
-def test_large_batch_invalid_cu_in_last_group_writes_nothing():
+@pytest.mark.parametrize("where", ["inside_last_group", "across_group_boundary"])
+def test_large_batch_cu_decrease(where):
+    """A decrease of cu_seq_lens in a batch run as several launches: the request
+    after it starts below an earlier boundary and is skipped (flag 8). Across a
+    group boundary, the earlier boundary belongs to the group before, so the
+    group launches must pass it on through the workspace."""
     wl = _large(2 * binding.MAX_REQS_PLAN + 100, 63)
     cu = wl.cu_seq_lens.numpy().copy()
-    cu[-20] = cu[-21] - 1  # one decrease, in the last group only
+    i = len(cu) - 20 if where == "inside_last_group" else 2 * binding.MAX_REQS_PLAN
+    cu[i] = cu[i - 1] - 1
+    assert cu[i + 1] > cu[i]  # the request starting at boundary i has rows
     _check(wl, cu=cu, expect_flag=og.BAD_CU, workspace=True)
-    # the verdict is cleared for the next call on the same workspace
+    # the workspace is left zeroed for the next call
     case = DeviceCase(wl, workspace=True)
     case.run()
     case.run()

@@ -3,8 +3,9 @@
 Each case plants one mistake in a temporary copy of oracle/pmg_oracle.c (an
 index off by one, a dropped seq_starts, a missing clamp at total_tokens, the
 wrong row stride, truncation or round-half-up instead of round-half-even, a
-wrong FP8 exponent bias or subnormal scale, a dropped dequant scale, a missing
-cu_seq_lens order check, an accepted negative start), builds it with gcc, and
+wrong FP8 exponent bias or subnormal scale, a dropped dequant scale, an
+accepted request whose rows start below an earlier cu_seq_lens boundary, an
+accepted negative start), builds it with gcc, and
 runs a battery of the pins against it: hand-worked golden cases, the numpy-only
 second route, closed forms, and the conversion checks against torch and
 numpy. Every mutant must fail at least one pin. The committed oracle is never
@@ -39,7 +40,9 @@ MUTANTS = {
     "e4m3 subnormal scale": ("mag = ldexpf((float)m, -9);", "mag = ldexpf((float)m, -10);"),
     "fp16 ties away from zero": ("if (rem > half || (rem == half && (q & 1u))) q += 1u;", "if (rem >= half) q += 1u;"),
     "dequant scale dropped": ("v = pmg_oracle_e4m3_to_f32(s[0]) * scale;", "v = pmg_oracle_e4m3_to_f32(s[0]) * 1.0f;"),
-    "cu order unchecked": ("if (cu_seq_lens[r + 1] < cu_seq_lens[r]) return O_BAD_CU;", ";"),
+    "rows below an earlier boundary accepted": ("if (len > 0 && ob < below) {",
+                                                "if (len > 0 && ob < below - 1000000) {"),
+    "earlier boundaries forgotten": ("if (ob > floor_row) floor_row = ob;", ";"),
     "negative start accepted": ("if (len > 0 && start < 0) {", "if (len > 0 && start < -1000000) {"),
     "token position off by one": ("const int64_t pos = t - first_row;", "const int64_t pos = t - first_row + 1;"),
     "token row range unchecked": ("if (t < first_row || t >= end_row) {", "if (t >= end_row + 1000000) {"),
