@@ -404,7 +404,10 @@ def run_per_config(args, dev, stream, world, headline=None):
         cold = r.cold()
         cold_clean = r.cold(read_back=True)
         r.check_flags()
+        tr = profiled_traffic(name)
         out[name] = {"workload": wl.name, "bytes_per_step": alg, "dtype": dtype_label(wl), "path": r.path,
+                     "dram_traffic_per_launch": None if tr is None else {"read": tr["read"], "write": tr["write"],
+                                                                         "source": tr["source"]},
                      "steady": {"gbs": round(alg / (ms * 1e-3) / 1e9, 1),
                                 "frac": round(alg / (ms * 1e-3) / 1e9 / peak, 4),
                                 "per_launch_us": round(ms * 1e3, 2), "steps_per_region": n,
