@@ -466,8 +466,11 @@ def run_ours(args, wl: W.Workload, ws: int, rank: int, local: int):
     cold_clean = None if args.quick else runner.cold(read_back=True)
     peak, peak_kind = measured_peak()
     achieved = alg_bytes / (per_launch_ms * 1e-3) / 1e9
+    tr_h = profiled_traffic(args.config) if args.entry == "gather" and args.options == 0 else None
     headline_entry = {"workload": wl.name, "bytes_per_step": alg_bytes, "dtype": dtype_label(wl),
                       "path": runner.path,
+                      "dram_traffic_per_launch": None if tr_h is None else {"read": tr_h["read"], "write": tr_h["write"],
+                                                                            "source": tr_h["source"]},
                       "steady": {"gbs": round(achieved, 1), "frac": round(achieved / peak, 4),
                                  "per_launch_us": round(per_launch_ms * 1e3, 2), "steps_per_region": args.steps,
                                  "regions": len(regions)},
