@@ -330,7 +330,7 @@ class Runner:
             torch.distributed.barrier()
         return reduce_max(a.elapsed_time(b), self.dev)
 
-    def cold(self, iters=30, read_back=False):
+    def cold(self, iters=50, read_back=False):
         """Median call time with L2 flushed before each call, outside the event
         pair: a 512 MB buffer is written (the page's cold-cache protocol), and
         with read_back it is then read back too, so that L2 holds clean lines
