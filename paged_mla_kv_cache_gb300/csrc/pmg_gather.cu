@@ -2055,13 +2055,16 @@ int bulk_stage_target_bytes() {
 }
 
 // Target bytes (of source rows) of one stage of the converting TMA ring;
-// PMG_CVT_STAGE_KB (4..48) overrides the default for tuning sweeps. 10 KB
-// stages leave room for five CTAs per SM, which measured best for fp8 rows
-// of 576 bytes (more CTAs in flight beat deeper rings).
+// PMG_CVT_STAGE_KB (4..48) overrides the default for tuning sweeps. The
+// converting kernel's registers allow four CTAs per SM; 12 KB stages let those
+// four fill shared memory with rings (about 194 KB of source in flight per
+// SM for fp8 rows of 576 bytes), which measured best: the bytes in flight per
+// SM decide, smaller stages (10 KB: 0.82 of peak on skew-8) and rings that cost
+// a CTA per SM (14 KB, 20 KB) lose.
 int cvt_stage_target_bytes() {
   static const int v = [] {
     const char* e = std::getenv("PMG_CVT_STAGE_KB");
-    int kb = e ? std::atoi(e) : 10;
+    int kb = e ? std::atoi(e) : 12;
     if (kb < 4) kb = 4;
     if (kb > kMaxStageBytes / 1024) kb = kMaxStageBytes / 1024;
     return kb * 1024;
