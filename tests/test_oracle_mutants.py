@@ -40,8 +40,8 @@ MUTANTS = {
     "e4m3 subnormal scale": ("mag = ldexpf((float)m, -9);", "mag = ldexpf((float)m, -10);"),
     "fp16 ties away from zero": ("if (rem > half || (rem == half && (q & 1u))) q += 1u;", "if (rem >= half) q += 1u;"),
     "dequant scale dropped": ("v = pmg_oracle_e4m3_to_f32(s[0]) * scale;", "v = pmg_oracle_e4m3_to_f32(s[0]) * 1.0f;"),
-    "rows below an earlier boundary accepted": ("if (len > 0 && ob < below) {",
-                                                "if (len > 0 && ob < below - 1000000) {"),
+    # (rows below row 0 stay refused: a mutant must not write outside its dst)
+    "rows below an earlier boundary accepted": ("if (len > 0 && ob < below) {", "if (len > 0 && ob < 0) {"),
     "earlier boundaries forgotten": ("if (ob > floor_row) floor_row = ob;", ";"),
     "negative start accepted": ("if (len > 0 && start < 0) {", "if (len > 0 && start < -1000000) {"),
     "token position off by one": ("const int64_t pos = t - first_row;", "const int64_t pos = t - first_row + 1;"),
@@ -78,6 +78,24 @@ def _id_cache(nb, B, E, rs=None):
     return (b << 20) | (s << 10) | e
 
 
+GUARD_ROWS = 64
+
+
+def _guarded(rows, cols, fill=0xA5A5A5A5):
+    """(buffer, view): a destination of `rows` rows inside GUARD_ROWS sentinel
+    rows on each side, so that a mutant that writes a row before 0 or past the
+    end writes into memory the test owns (and fails the guard check) instead of
+    corrupting the heap."""
+    buf = np.full((rows + 2 * GUARD_ROWS, cols), 0x5A5A5A5A, np.uint32)
+    view = buf[GUARD_ROWS:GUARD_ROWS + rows]
+    view[:] = fill
+    return buf, view
+
+
+def _guards_intact(buf):
+    return bool(np.all(buf[:GUARD_ROWS] == 0x5A5A5A5A)) and bool(np.all(buf[-GUARD_ROWS:] == 0x5A5A5A5A))
+
+
 def _pin_hand_cases():
     for c in json.load(open(GOLDEN))["cases"]:
         if "rows" not in c:
@@ -86,11 +104,11 @@ def _pin_hand_cases():
         cache = _id_cache(c["num_blocks"], c["block_size"], E)
         cu = np.array(c["cu_seq_lens"], np.int32)
         T = c["total_tokens"]
-        dst = np.full((T, E), 0xA5A5A5A5, np.uint32)
+        buf, dst = _guarded(T, E)
         ss = None if c["seq_starts"] is None else np.array(c["seq_starts"], np.int32)
         flag = og.gather(cache, np.array(c["block_table"], np.int32), cu, ss, len(cu) - 1, T, c["block_size"], E,
                          "fp32", "fp32", 1.0, dst)
-        if flag != c["flag"]:
+        if flag != c["flag"] or not _guards_intact(buf):
             return False
         for i, want in enumerate(c["rows"]):
             if want is None:
@@ -118,8 +136,10 @@ def _pin_library_route():
         cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
         T = int(cu[-1])
         cache = _id_cache(nb, B, E)
-        dst = np.full((T, E), 0xA5A5A5A5, np.uint32)
+        buf, dst = _guarded(T, E)
         if og.gather(cache, bt, cu, np.array(starts, np.int32), R, T, B, E, "fp32", "fp32", 1.0, dst) != 0:
+            return False
+        if not _guards_intact(buf):
             return False
         for r in range(R):
             if lens[r] == 0:
@@ -132,9 +152,11 @@ def _pin_library_route():
 
 def _pin_padded_and_clamp():
     cache = _id_cache(3, 4, 3, rs=5)
-    dst = np.full((10, 6), 0xA5A5A5A5, np.uint32)
+    gbuf, dst = _guarded(10, 6)
     og.gather(cache, np.array([[2, 0, 1]], np.int32), np.array([0, 10], np.int32), np.array([1], np.int32), 1, 10,
               4, 3, "fp32", "fp32", 1.0, dst)
+    if not _guards_intact(gbuf):
+        return False
     for i in range(10):
         p = 1 + i
         if not np.array_equal(dst[i, :3], cache[[2, 0, 1][p // 4], p % 4, :3]) or not np.all(dst[i, 3:] == 0xA5A5A5A5):
@@ -191,10 +213,10 @@ def _pin_token_cases():
         cache = _id_cache(c["num_blocks"], c["block_size"], E)
         t2s = np.array(c["token_to_seq"], np.int32)
         cu = np.array(c["cu_seq_lens"], np.int32)
-        dst = np.full((len(t2s), E), 0xA5A5A5A5, np.uint32)
+        buf, dst = _guarded(len(t2s), E)
         flag = og.gather_tokens(cache, np.array(c["block_table"], np.int32), t2s, cu, len(cu) - 1, len(t2s),
                                 c["block_size"], E, "fp32", "fp32", 1.0, dst)
-        if flag != c["flag"]:
+        if flag != c["flag"] or not _guards_intact(buf):
             return False
         for i, want in enumerate(c["rows"]):
             if want is None:
