@@ -2041,17 +2041,28 @@ int conv_of(int src, int dst) {
   return -1;
 }
 
-// Target bytes of one TMA ring stage. PMG_BULK_STAGE_KB (8..48) overrides the
-// default for tuning sweeps; it changes only the chunking, never the result.
-int bulk_stage_target_bytes() {
-  static const int v = [] {
+// Target bytes of one stage of the byte-copy TMA ring (three stages by
+// default). A page gather over back-to-back source rows moves each chunk with
+// one copy: 32 KB stages, two CTAs per SM. Padded source rows take one copy per
+// row, all issued by the CTA's one producer thread, and the per-token mode
+// resolves its rows through three dependent reads per batch: both do better
+// with 22 KB stages, which fit three CTAs (three producers and schedulers) per
+// SM. Measured: single-300K 1.008 -> 1.010, single-60K 0.926 -> 0.931,
+// skew-64 raw (padded) 0.961 -> 0.983, per-token single-60K 0.86 -> 0.93 of
+// the copy peak, against four 24 KB stages. PMG_BULK_STAGE_KB (8..48)
+// overrides both for tuning sweeps; it changes only the chunking, never the
+// result.
+int bulk_stage_target_bytes(bool one_copy_per_chunk) {
+  static const int env = [] {
     const char* e = std::getenv("PMG_BULK_STAGE_KB");
-    int kb = e ? std::atoi(e) : 24;
+    if (e == nullptr) return 0;
+    int kb = std::atoi(e);
     if (kb < 8) kb = 8;
     if (kb > kMaxStageBytes / 1024) kb = kMaxStageBytes / 1024;
     return kb * 1024;
   }();
-  return v;
+  if (env > 0) return env;
+  return (one_copy_per_chunk ? 32 : 22) * 1024;
 }
 
 // Target bytes (of source rows) of one stage of the converting TMA ring;
@@ -2112,7 +2123,7 @@ int sched_min_rows() {
 
 // Ring depths (PMG_BULK_STAGES, PMG_CVT_STAGES: 2..8) for tuning sweeps.
 int bulk_stages() {
-  static const int v = env_int("PMG_BULK_STAGES", 4, 2, kMaxStages);
+  static const int v = env_int("PMG_BULK_STAGES", 3, 2, kMaxStages);
   return v;
 }
 int cvt_stages() {
@@ -2172,6 +2183,15 @@ int unit_candidates(int conv, int* out) {
     case CONV_E4M3_F32: out[0] = 16; out[1] = 4; out[2] = 1; return 3;
     default: out[0] = 8; out[1] = 2; out[2] = 1; return 3;
   }
+}
+
+// Ring of the byte-copy kernel: stages of whole rows.
+void set_bulk_ring(Params& q, bool one_copy_per_chunk) {
+  const int32_t rows = std::max(1, bulk_stage_target_bytes(one_copy_per_chunk) / q.row_src_bytes);
+  q.rows_per_stage = rows;
+  q.stage_bytes = rows * q.row_src_bytes;
+  q.stages = bulk_stages();
+  q.prefetch_rows = prefetch_stages() * rows;
 }
 
 // Validation and path choice: the host half of every entry point. No CUDA call.
@@ -2253,12 +2273,7 @@ int make_plan(const void* cache, int64_t cbs, int64_t cts, int64_t num_blocks, c
   q.dst_dense = q.dst_stride_b == q.row_dst_bytes;
   if (bulk_ok) {
     out.path = PMG_PATH_BULK;
-    // ring stages of whole rows
-    const int32_t rows = std::max(1, bulk_stage_target_bytes() / q.row_src_bytes);
-    q.rows_per_stage = rows;
-    q.stage_bytes = rows * q.row_src_bytes;
-    q.stages = bulk_stages();
-    q.prefetch_rows = prefetch_stages() * rows;
+    set_bulk_ring(q, q.src_dense != 0);
     out.unit = 0;
   } else {
     int64_t upr;
@@ -2661,6 +2676,7 @@ int pmg_gather_tokens(const void* cache, int64_t cache_block_stride, int64_t cac
       pl.prm.R = num_reqs;
       pl.prm.t2s = token_to_seq;
       pl.prm.token_mode = 1;
+      if (pl.conv == CONV_COPY) set_bulk_ring(pl.prm, false);  // per-token rows: the smaller ring stages
       return launch_one(pl, static_cast<cudaStream_t>(stream));
     }
   }
