@@ -112,6 +112,7 @@ struct Params {
   int32_t token_mode;     // 1: rows [0, T) map through t2s instead of the page plan
   int32_t sched_static_pct;  // dynamic mode: share of rows split statically up front
   int32_t sched_min_rows;    // dynamic mode only when rows per CTA reach this
+  int32_t sched_head_stages; // dynamic mode: static share of at least this many ring stages per CTA
   // SIMT mover
   int32_t units_per_row;  // entry_size / elements per unit
   uint32_t upr_magic;     // fast division by units_per_row (fast_div)
@@ -747,10 +748,11 @@ struct Items {
 
 // Dynamic mode needs a workspace and enough rows per CTA for the claims to
 // pay off. Each CTA's static share is sched_static_pct % of its rows, but at
-// least two ring stages (or all of its rows): the static item starts the
-// moment the launch may read the cache, while a claimed item waits for its
-// claim, so a CTA with little work needs a static head start covering that
-// latency (skew-8: 60 rows per CTA, 0.77 -> 0.81 of peak). Dynamic items are
+// least sched_head_stages ring stages (or all of its rows): the static item
+// starts the moment the launch may read the cache, while a claimed item waits
+// for its claim, so a CTA needs a static head start covering that latency
+// (four stages for a page gather, two in token mode; the host sets them from
+// measurements). Dynamic items are
 // about rows / (64 G) rows and never smaller than one ring stage: small items
 // even out the CTAs' finishing times (single-300K 0.975 -> 0.988), but an item
 // must carry more data than the claim and block-table round trips that fetch
@@ -767,7 +769,8 @@ __device__ __forceinline__ Items make_items(const PlanView& v, const Params& p) 
   if (it.dynamic) {
     it.a = static_cast<uint32_t>(static_cast<uint64_t>(rows) * static_cast<uint32_t>(p.sched_static_pct) / 100u / G);
     const uint32_t rps = static_cast<uint32_t>(p.rows_per_stage > 0 ? p.rows_per_stage : 1);
-    const uint32_t head = 2u * rps < rows / G ? 2u * rps : rows / G;
+    const uint32_t hs = static_cast<uint32_t>(p.sched_head_stages) * rps;
+    const uint32_t head = hs < rows / G ? hs : rows / G;
     if (it.a < head) it.a = head;
     const uint32_t d = rows / ((p.token_mode ? 16u : 64u) * G);
     const uint32_t dmin = static_cast<uint32_t>(p.rows_per_stage > 0 ? p.rows_per_stage : 1);
@@ -2065,22 +2068,25 @@ int bulk_stage_target_bytes(bool one_copy_per_chunk) {
   return (one_copy_per_chunk ? 32 : 22) * 1024;
 }
 
-// Target bytes (of source rows) of one stage of the converting TMA ring;
-// PMG_CVT_STAGE_KB (4..48) overrides the default for tuning sweeps. The
-// converting kernel's registers allow four CTAs per SM; 12 KB stages let those
-// four fill shared memory with rings (about 194 KB of source in flight per
-// SM for fp8 rows of 576 bytes), which measured best: the bytes in flight per
-// SM decide, smaller stages (10 KB: 0.82 of peak on skew-8) and rings that cost
-// a CTA per SM (14 KB, 20 KB) lose.
-int cvt_stage_target_bytes() {
-  static const int v = [] {
+// Ring of the converting kernel. Its registers allow four CTAs per SM, and
+// what decides is the source bytes in flight per SM: rings that let those four
+// fill shared memory (about 194 KB for fp8 rows of 576 bytes) measured best,
+// smaller ones (4 x 10 KB: 0.82 of peak on skew-8) and ones that cost a CTA per
+// SM (4 x 14 KB, 4 x 20 KB) less. A page gather takes three 16 KB stages
+// (skew-64 dequant 0.943 against 0.932 with four of 12 KB), the per-token mode
+// four of 12 KB (its scheduler's dependent reads favour it: 0.93 against 0.92).
+// PMG_CVT_STAGE_KB (4..48) and PMG_CVT_STAGES override both for tuning sweeps.
+int cvt_stage_target_bytes(bool token_mode) {
+  static const int env = [] {
     const char* e = std::getenv("PMG_CVT_STAGE_KB");
-    int kb = e ? std::atoi(e) : 12;
+    if (e == nullptr) return 0;
+    int kb = std::atoi(e);
     if (kb < 4) kb = 4;
     if (kb > kMaxStageBytes / 1024) kb = kMaxStageBytes / 1024;
     return kb * 1024;
   }();
-  return v;
+  if (env > 0) return env;
+  return (token_mode ? 12 : 16) * 1024;
 }
 
 // Dynamic scheduling knobs (PMG_SCHED_STATIC_PCT, PMG_SCHED_MIN_ROWS) for
@@ -2120,15 +2126,26 @@ int sched_min_rows() {
   static const int v = env_int("PMG_SCHED_MIN_ROWS", 32, 1, 1 << 30);
   return v;
 }
+// Static head of the dynamic split, in ring stages per CTA: a page gather's
+// CTAs start with at least four stages of their own rows before they claim
+// (single-60K 0.936 -> 0.974 of peak; the large workloads unchanged), the
+// per-token mode with two (its claims cost less than its idle head: four
+// stages lost 8% on skew-8). PMG_SCHED_HEAD_STAGES overrides both.
+int sched_head_stages(bool token_mode) {
+  static const int v = env_int("PMG_SCHED_HEAD_STAGES", 0, 0, 64);
+  if (v >= 1) return v;
+  return token_mode ? 2 : 4;
+}
 
 // Ring depths (PMG_BULK_STAGES, PMG_CVT_STAGES: 2..8) for tuning sweeps.
 int bulk_stages() {
   static const int v = env_int("PMG_BULK_STAGES", 3, 2, kMaxStages);
   return v;
 }
-int cvt_stages() {
-  static const int v = env_int("PMG_CVT_STAGES", 4, 2, kMaxStages);
-  return v;
+int cvt_stages(bool token_mode) {
+  static const int v = env_int("PMG_CVT_STAGES", 0, 0, kMaxStages);
+  if (v >= 2) return v;
+  return token_mode ? 4 : 3;
 }
 
 // Elements per unit of the converting TMA path: one 16-byte store per unit.
@@ -2183,6 +2200,15 @@ int unit_candidates(int conv, int* out) {
     case CONV_E4M3_F32: out[0] = 16; out[1] = 4; out[2] = 1; return 3;
     default: out[0] = 8; out[1] = 2; out[2] = 1; return 3;
   }
+}
+
+// Ring of the converting kernel: stages of whole source rows.
+void set_cvt_ring(Params& q, bool token_mode) {
+  const int32_t rows = std::max(1, cvt_stage_target_bytes(token_mode) / q.row_src_bytes);
+  q.rows_per_stage = rows;
+  q.stage_bytes = rows * q.row_src_bytes;
+  q.stages = cvt_stages(token_mode);
+  q.prefetch_rows = prefetch_stages() * rows;
 }
 
 // Ring of the byte-copy kernel: stages of whole rows.
@@ -2254,6 +2280,7 @@ int make_plan(const void* cache, int64_t cbs, int64_t cts, int64_t num_blocks, c
   q.spec_guess = use_spec_guess() ? 1 : 0;
   q.sched_static_pct = sched_static_pct();
   q.sched_min_rows = sched_min_rows();
+  q.sched_head_stages = sched_head_stages(false);
   out.conv = conv;
 
   int unit = pick_unit(conv, es, ed, E, cache, q.blk_stride_b, q.tok_stride_b, dst, q.dst_stride_b);
@@ -2281,11 +2308,7 @@ int make_plan(const void* cache, int64_t cbs, int64_t cts, int64_t num_blocks, c
       out.path = PMG_PATH_BULK;
       out.unit = cu_unit;
       upr = E / cu_unit;
-      const int32_t rows = std::max(1, cvt_stage_target_bytes() / q.row_src_bytes);
-      q.rows_per_stage = rows;
-      q.stage_bytes = rows * q.row_src_bytes;
-      q.stages = cvt_stages();
-      q.prefetch_rows = prefetch_stages() * rows;
+      set_cvt_ring(q, false);
       q.dense = q.dst_dense;
     } else {
       const int64_t unit_elems = (conv == CONV_COPY) ? unit / es : unit;
@@ -2676,7 +2699,10 @@ int pmg_gather_tokens(const void* cache, int64_t cache_block_stride, int64_t cac
       pl.prm.R = num_reqs;
       pl.prm.t2s = token_to_seq;
       pl.prm.token_mode = 1;
-      if (pl.conv == CONV_COPY) set_bulk_ring(pl.prm, false);  // per-token rows: the smaller ring stages
+      // the per-token mode's own ring sizes and static head
+      if (pl.conv == CONV_COPY) set_bulk_ring(pl.prm, false);
+      else set_cvt_ring(pl.prm, true);
+      pl.prm.sched_head_stages = sched_head_stages(true);
       return launch_one(pl, static_cast<cudaStream_t>(stream));
     }
   }
