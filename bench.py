@@ -236,6 +236,17 @@ def dtype_label(wl: W.Workload) -> str:
     return wl.src_dtype if wl.src_dtype == wl.dst_dtype else f"{wl.src_dtype}->{wl.dst_dtype}"
 
 
+def kernel_of(path: str, wl: W.Workload, entry: str) -> str:
+    """The kernel a call on this path launches: the TMA path ("bulk") has a
+    byte-copy kernel and a converting kernel; the SIMT paths one kernel per
+    entry point."""
+    if path == "bulk":
+        return "gather_bulk_kernel" if wl.src_dtype == wl.dst_dtype else "gather_tma_convert_kernel"
+    if path == "none":
+        return "none"
+    return "gather_tokens_kernel" if entry == "tokens" else "gather_simt_kernel"
+
+
 class DeviceInputs:
     """One replica of a workload's inputs and output, resident on the device."""
 
@@ -275,6 +286,7 @@ class Runner:
         path, _ = binding.select_path(base.cache, base.dst, base.bt, base.cu, num_reqs=wl.num_reqs,
                                       options=args.options)
         self.path = ("per-token " + path) if args.entry == "tokens" else path
+        self.kernel = kernel_of(path, wl, args.entry)
 
     def footprint_mb(self):
         return sum(r.nbytes() for r in self.reps) / 1e6
@@ -353,7 +365,8 @@ class Runner:
         med = statistics.median(times)
         alg = self.wl.algorithmic_bytes()
         peak, _ = measured_peak()
-        return {"median_us": round(med * 1e3, 2), "p10_us": round(times[len(times) // 10] * 1e3, 2),
+        return {"median_us": round(med * 1e3, 2), "mean_us": round(statistics.fmean(times) * 1e3, 2),
+                "p10_us": round(times[len(times) // 10] * 1e3, 2),
                 "p90_us": round(times[(9 * len(times)) // 10] * 1e3, 2), "iters": iters,
                 "gbs": round(alg / (med * 1e-3) / 1e9, 1), "frac": round(alg / (med * 1e-3) / 1e9 / peak, 4),
                 "flush": ("512 MB written then read back" if read_back else "512 MB written")
@@ -406,6 +419,7 @@ def run_per_config(args, dev, stream, world, headline=None):
         r.check_flags()
         tr = profiled_traffic(name)
         out[name] = {"workload": wl.name, "bytes_per_step": alg, "dtype": dtype_label(wl), "path": r.path,
+                     "kernel": r.kernel,
                      "dram_traffic_per_launch": None if tr is None else {"read": tr["read"], "write": tr["write"],
                                                                          "source": tr["source"]},
                      "steady": {"gbs": round(alg / (ms * 1e-3) / 1e9, 1),
@@ -468,7 +482,7 @@ def run_ours(args, wl: W.Workload, ws: int, rank: int, local: int):
     achieved = alg_bytes / (per_launch_ms * 1e-3) / 1e9
     tr_h = profiled_traffic(args.config) if args.entry == "gather" and args.options == 0 else None
     headline_entry = {"workload": wl.name, "bytes_per_step": alg_bytes, "dtype": dtype_label(wl),
-                      "path": runner.path,
+                      "path": runner.path, "kernel": runner.kernel,
                       "dram_traffic_per_launch": None if tr_h is None else {"read": tr_h["read"], "write": tr_h["write"],
                                                                             "source": tr_h["source"]},
                       "steady": {"gbs": round(achieved, 1), "frac": round(achieved / peak, 4),
@@ -504,6 +518,7 @@ def run_ours(args, wl: W.Workload, ws: int, rank: int, local: int):
         "data": "synthetic (seeded N(0,1) cache, seeded block-id permutation)",
         "config": workload_config(wl),
         "path": runner.path if args.options == 0 else f"{runner.path} (options {args.options})",
+        "kernel": runner.kernel,
         "schedule": ("static" if args.no_workspace else "dynamic (workspace)")
                     + (", early metadata" if args.early_metadata else ""),
         "parallelism": f"replicas x{ws}",
