@@ -113,6 +113,8 @@ struct Params {
   int32_t sched_static_pct;  // dynamic mode: share of rows split statically up front
   int32_t sched_min_rows;    // dynamic mode only when rows per CTA reach this
   int32_t sched_head_stages; // dynamic mode: static share of at least this many ring stages per CTA
+  int32_t sched_tilt_pct;    // static shares fall linearly with blockIdx: first (1 + t), last (1 - t) of even
+  int32_t sched_tilt_pow;     // shape of the tilt: shares 1 + t (1 - (pow + 1) x^pow), x = blockIdx / grid
   // SIMT mover
   int32_t units_per_row;  // entry_size / elements per unit
   uint32_t upr_magic;     // fast division by units_per_row (fast_div)
@@ -739,10 +741,16 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 // resets the counter for the next call.
 // ---------------------------------------------------------------------------
 
+// Largest grid for which tilted static shares are computed (the numerator of
+// tilted_prefix stays exact in 64 bits); larger grids split evenly.
+constexpr uint32_t kTiltMaxGrid = 2048;
+
 struct Items {
   uint32_t lo, hi;  // output rows [lo, hi)
   uint32_t a, d;    // static share and dynamic item size
   uint32_t n;       // number of items
+  uint32_t tilt;    // percent: static shares tilted towards low blockIdx (0: even)
+  uint32_t tilt_pow;
   bool dynamic;
 };
 
@@ -765,28 +773,69 @@ __device__ __forceinline__ Items make_items(const PlanView& v, const Params& p) 
   it.hi = p.token_mode ? static_cast<uint32_t>(p.T) : static_cast<uint32_t>(v.ob[p.R]);
   const uint32_t rows = it.hi - it.lo;
   const uint32_t G = gridDim.x;
-  it.dynamic = p.sched != nullptr && rows / G >= static_cast<uint32_t>(p.sched_min_rows);
+  const bool big = rows / G >= static_cast<uint32_t>(p.sched_min_rows);
+  const uint32_t rps = static_cast<uint32_t>(p.rows_per_stage > 0 ? p.rows_per_stage : 1);
+  const uint32_t hs = static_cast<uint32_t>(p.sched_head_stages) * rps;
+  it.dynamic = p.sched != nullptr && big;
   if (it.dynamic) {
     it.a = static_cast<uint32_t>(static_cast<uint64_t>(rows) * static_cast<uint32_t>(p.sched_static_pct) / 100u / G);
-    const uint32_t rps = static_cast<uint32_t>(p.rows_per_stage > 0 ? p.rows_per_stage : 1);
-    const uint32_t hs = static_cast<uint32_t>(p.sched_head_stages) * rps;
     const uint32_t head = hs < rows / G ? hs : rows / G;
     if (it.a < head) it.a = head;
     const uint32_t d = rows / ((p.token_mode ? 16u : 64u) * G);
-    const uint32_t dmin = static_cast<uint32_t>(p.rows_per_stage > 0 ? p.rows_per_stage : 1);
-    it.d = d > dmin ? d : dmin;
+    it.d = d > rps ? d : rps;
     const uint32_t rest = rows - G * it.a;
     it.n = G + (rest + it.d - 1u) / it.d;
   } else {
     it.a = it.d = 0;
     it.n = G;
   }
+  // The tilt only where claims cannot even out the finishing times: fewer
+  // dynamic items than CTAs, or a static split of at most the head plus one
+  // stage per CTA (the late CTAs' lag is a few microseconds whatever the
+  // launch's length, so longer static launches keep even shares). And only
+  // where CTAs hold enough rows for their start-up not to dominate. Shares
+  // stay >= 0 (F increasing) while tilt * pow <= 100.
+  const bool few = it.dynamic ? it.n - G < G : rows / G < hs + rps;
+  it.tilt_pow = p.sched_tilt_pow >= 1 && p.sched_tilt_pow <= 4 ? static_cast<uint32_t>(p.sched_tilt_pow) : 1u;
+  const uint32_t tmax = 100u / it.tilt_pow;
+  const uint32_t t = static_cast<uint32_t>(p.sched_tilt_pct);
+  it.tilt = (G <= kTiltMaxGrid && big && few) ? (t < tmax ? t : tmax) : 0u;
   return it;
+}
+
+// Rows before CTA k when `total` rows are split over G CTAs with shares
+// 1 + t (1 - (q + 1) x^q) of the even share (x = k / G, t = tilt / 100,
+// q = pow in 1..4): about total * F(k / G) with F(x) = x + t (x - x^(q+1)).
+// q = 1 falls linearly from 1 + t to 1 - t; larger q keep the shares near
+// 1 + t longer and drop them towards the last CTAs. The numerator
+// k (100 G^q + tilt (G^q - k^q)) is exact in 64 bits for G <= 2048 and grows
+// with k; scaling it in single precision keeps that order (rounding is
+// monotone), k = G gives the total, and CTA k's end and CTA k + 1's start are
+// the same call: the ranges are contiguous, in order and cover every row once.
+__device__ __forceinline__ uint32_t tilted_prefix(uint32_t total, uint32_t k, uint32_t G, uint32_t tilt,
+                                                  uint32_t pw) {
+  if (k >= G) return total;
+  uint64_t gq = G, kq = k;
+  for (uint32_t i = 1; i < pw; ++i) {
+    gq *= G;
+    kq *= k;
+  }
+  const uint64_t num = static_cast<uint64_t>(k) * (gq * 100u + static_cast<uint64_t>(tilt) * (gq - kq));
+  const float scale = static_cast<float>(total) / (static_cast<float>(gq) * static_cast<float>(G) * 100.0f);
+  const float x = static_cast<float>(num) * scale;
+  const uint32_t v = x >= static_cast<float>(total) ? total : static_cast<uint32_t>(x);
+  return v < total ? v : total;
 }
 
 __device__ __forceinline__ void item_rows(const Items& it, uint32_t k, uint32_t& r0, uint32_t& r1) {
   const uint32_t G = gridDim.x;
-  if (!it.dynamic) {
+  if (it.tilt != 0u && k < G) {
+    // CTAs start in blockIdx order as the previous grid's CTAs leave: the
+    // late ones get less of the static rows
+    const uint32_t total = it.dynamic ? G * it.a : it.hi - it.lo;
+    r0 = it.lo + tilted_prefix(total, k, G, it.tilt, it.tilt_pow);
+    r1 = it.lo + tilted_prefix(total, k + 1u, G, it.tilt, it.tilt_pow);
+  } else if (!it.dynamic) {
     const uint32_t rows = it.hi - it.lo;
     const uint32_t per = rows / G;
     const uint32_t rem = rows - per * G;
@@ -2137,6 +2186,27 @@ int sched_head_stages(bool token_mode) {
   return token_mode ? 2 : 4;
 }
 
+// Tilt of the static shares by blockIdx (make_items, tilted_prefix). A
+// launch's CTAs start in blockIdx order as the previous grid's CTAs leave (the
+// last eighth about 5 us after the first in steady state), and the late ones
+// pay their start-up (plan, block-table and first data round trips) while the
+// others already stream. The converting kernel takes a cubic tilt of 10%
+// (shares about 1.1 of even for most CTAs, falling to 0.6 for the last):
+// skew-8 0.821 -> 0.870 and 0.832 -> 0.876 of the copy peak on two boxes, one
+// fp8 request of 45,657 tokens 0.910 -> 0.937; linear tilts of 20-30% reached
+// 0.864. The byte-copy kernel keeps even shares (a tilt cost its static splits
+// 1-3.5%). PMG_SCHED_TILT_PCT (0..100) and PMG_SCHED_TILT_POW (1..4) override
+// both kernels for tuning sweeps.
+int sched_tilt_pct(bool converter) {
+  static const int v = env_int("PMG_SCHED_TILT_PCT", -1, -1, 100);
+  if (v >= 0) return v;
+  return converter ? 10 : 0;
+}
+int sched_tilt_pow() {
+  static const int v = env_int("PMG_SCHED_TILT_POW", 3, 1, 4);
+  return v;
+}
+
 // Ring depths (PMG_BULK_STAGES, PMG_CVT_STAGES: 2..8) for tuning sweeps.
 int bulk_stages() {
   static const int v = env_int("PMG_BULK_STAGES", 3, 2, kMaxStages);
@@ -2281,6 +2351,7 @@ int make_plan(const void* cache, int64_t cbs, int64_t cts, int64_t num_blocks, c
   q.sched_static_pct = sched_static_pct();
   q.sched_min_rows = sched_min_rows();
   q.sched_head_stages = sched_head_stages(false);
+  q.sched_tilt_pow = sched_tilt_pow();
   out.conv = conv;
 
   int unit = pick_unit(conv, es, ed, E, cache, q.blk_stride_b, q.tok_stride_b, dst, q.dst_stride_b);
@@ -2301,6 +2372,7 @@ int make_plan(const void* cache, int64_t cbs, int64_t cts, int64_t num_blocks, c
   if (bulk_ok) {
     out.path = PMG_PATH_BULK;
     set_bulk_ring(q, q.src_dense != 0);
+    q.sched_tilt_pct = sched_tilt_pct(false);
     out.unit = 0;
   } else {
     int64_t upr;
@@ -2309,6 +2381,7 @@ int make_plan(const void* cache, int64_t cbs, int64_t cts, int64_t num_blocks, c
       out.unit = cu_unit;
       upr = E / cu_unit;
       set_cvt_ring(q, false);
+      q.sched_tilt_pct = sched_tilt_pct(true);
       q.dense = q.dst_dense;
     } else {
       const int64_t unit_elems = (conv == CONV_COPY) ? unit / es : unit;
