@@ -2093,6 +2093,13 @@ int conv_of(int src, int dst) {
   return -1;
 }
 
+// An integer tuning variable from the environment, clamped to [lo, hi].
+int env_int(const char* name, int dflt, int lo, int hi) {
+  const char* e = std::getenv(name);
+  int v = e ? std::atoi(e) : dflt;
+  return v < lo ? lo : (v > hi ? hi : v);
+}
+
 // Target bytes of one stage of the byte-copy TMA ring (three stages by
 // default). A page gather over back-to-back source rows moves each chunk with
 // one copy: 32 KB stages, two CTAs per SM. Padded source rows take one copy per
@@ -2117,34 +2124,51 @@ int bulk_stage_target_bytes(bool one_copy_per_chunk) {
   return (one_copy_per_chunk ? 32 : 22) * 1024;
 }
 
-// Ring of the converting kernel. Its registers allow four CTAs per SM, and
-// what decides is the source bytes in flight per SM: rings that let those four
-// fill shared memory (about 194 KB for fp8 rows of 576 bytes) measured best,
-// smaller ones (4 x 10 KB: 0.82 of peak on skew-8) and ones that cost a CTA per
-// SM (4 x 14 KB, 4 x 20 KB) less. A page gather takes three 16 KB stages
-// (skew-64 dequant 0.943 against 0.932 with four of 12 KB), the per-token mode
-// four of 12 KB (its scheduler's dependent reads favour it: 0.93 against 0.92).
-// PMG_CVT_STAGE_KB (4..48) and PMG_CVT_STAGES override both for tuning sweeps.
-int cvt_stage_target_bytes(bool token_mode) {
-  static const int env = [] {
+// Ring of the converting kernel. Its registers allow four CTAs per SM; what
+// decides is the source bytes in flight per SM and how the ring's stages fall
+// against the work split. Measured on single fp8 -> bf16 requests and the
+// named workloads (fractions of the copy peak):
+// - launches of at most 128 rows per CTA (a static split: each CTA's head of
+//   four stages covers its share) take two 18 KB stages of 32 rows: skew-8
+//   0.875 -> 0.892, one 60,000-token request 0.968 -> 0.979, against three of
+//   16 KB; longer launches lose with two stages (120,000 tokens 0.93);
+// - longer launches over back-to-back rows take three 14 KB stages (120,000
+//   tokens 0.940 -> 0.973, 300,000 0.989 -> 0.999);
+// - longer launches over padded rows keep three 16 KB stages (skew-64 dequant
+//   0.940; 0.929-0.938 with 4 x 12, 3 x 14, 3 x 18 or 2 x 18 KB);
+// - the per-token mode four of 12 KB (its scheduler's dependent reads favour
+//   it: 0.93 against 0.92).
+// rows_per_cta < 0 means not known yet (the host half of a call, before the
+// grid is sized). PMG_CVT_STAGE_KB (4..48) and PMG_CVT_STAGES (2..8) override
+// every case for tuning sweeps.
+constexpr int64_t kCvtSmallRows = 128;
+constexpr int kCvtCtasPerSm = 4;
+struct CvtRing {
+  int stages;
+  int kb;
+};
+CvtRing cvt_ring(bool token_mode, bool dense_rows, int64_t rows_per_cta) {
+  static const int env_kb = [] {
     const char* e = std::getenv("PMG_CVT_STAGE_KB");
     if (e == nullptr) return 0;
     int kb = std::atoi(e);
     if (kb < 4) kb = 4;
     if (kb > kMaxStageBytes / 1024) kb = kMaxStageBytes / 1024;
-    return kb * 1024;
+    return kb;
   }();
-  if (env > 0) return env;
-  return (token_mode ? 12 : 16) * 1024;
+  static const int env_stages = env_int("PMG_CVT_STAGES", 0, 0, kMaxStages);
+  CvtRing r;
+  if (token_mode) r = {4, 12};
+  else if (rows_per_cta >= 0 && rows_per_cta <= kCvtSmallRows) r = {2, 18};
+  else if (dense_rows) r = {3, 14};
+  else r = {3, 16};
+  if (env_kb > 0) r.kb = env_kb;
+  if (env_stages >= 2) r.stages = env_stages;
+  return r;
 }
 
 // Dynamic scheduling knobs (PMG_SCHED_STATIC_PCT, PMG_SCHED_MIN_ROWS) for
 // tuning sweeps; they change only the work split, never the result.
-int env_int(const char* name, int dflt, int lo, int hi) {
-  const char* e = std::getenv(name);
-  int v = e ? std::atoi(e) : dflt;
-  return v < lo ? lo : (v > hi ? hi : v);
-}
 int sched_static_pct() {
   static const int v = env_int("PMG_SCHED_STATIC_PCT", 25, 0, 100);
   return v;
@@ -2212,11 +2236,6 @@ int bulk_stages() {
   static const int v = env_int("PMG_BULK_STAGES", 3, 2, kMaxStages);
   return v;
 }
-int cvt_stages(bool token_mode) {
-  static const int v = env_int("PMG_CVT_STAGES", 0, 0, kMaxStages);
-  if (v >= 2) return v;
-  return token_mode ? 4 : 3;
-}
 
 // Elements per unit of the converting TMA path: one 16-byte store per unit.
 int tma_convert_unit(int conv) {
@@ -2273,11 +2292,12 @@ int unit_candidates(int conv, int* out) {
 }
 
 // Ring of the converting kernel: stages of whole source rows.
-void set_cvt_ring(Params& q, bool token_mode) {
-  const int32_t rows = std::max(1, cvt_stage_target_bytes(token_mode) / q.row_src_bytes);
+void set_cvt_ring(Params& q, bool token_mode, int64_t rows_per_cta) {
+  const CvtRing r = cvt_ring(token_mode, q.src_dense != 0, rows_per_cta);
+  const int32_t rows = std::max(1, r.kb * 1024 / q.row_src_bytes);
   q.rows_per_stage = rows;
   q.stage_bytes = rows * q.row_src_bytes;
-  q.stages = cvt_stages(token_mode);
+  q.stages = r.stages;
   q.prefetch_rows = prefetch_stages() * rows;
 }
 
@@ -2380,7 +2400,7 @@ int make_plan(const void* cache, int64_t cbs, int64_t cts, int64_t num_blocks, c
       out.path = PMG_PATH_BULK;
       out.unit = cu_unit;
       upr = E / cu_unit;
-      set_cvt_ring(q, false);
+      set_cvt_ring(q, false, -1);  // sized again at launch, from the grid
       q.sched_tilt_pct = sched_tilt_pct(true);
       q.dense = q.dst_dense;
     } else {
@@ -2570,6 +2590,12 @@ int launch_one(const Plan& pl, cudaStream_t stream) {
   const int64_t max_by_rows = (static_cast<int64_t>(q.T) + kMinRowsPerCta - 1) / kMinRowsPerCta;
   if (pl.path == PMG_PATH_BULK) {
     const bool copy = pl.conv == CONV_COPY;
+    if (!copy && !q.token_mode) {
+      // the converter's ring depends on the rows each CTA will hold
+      const int64_t ctas = std::max<int64_t>(1, std::min<int64_t>(static_cast<int64_t>(kCvtCtasPerSm) * sms,
+                                                                  max_by_rows));
+      set_cvt_ring(q, false, static_cast<int64_t>(q.T) / ctas);
+    }
     KernelFn k = copy ? gather_bulk_kernel : tma_convert_kernel_for(pl.conv);
     if (k == nullptr) return PMG_ERR_UNSUPPORTED;
     const int threads = copy ? kBulkThreads : kCvtThreads;
@@ -2774,7 +2800,7 @@ int pmg_gather_tokens(const void* cache, int64_t cache_block_stride, int64_t cac
       pl.prm.token_mode = 1;
       // the per-token mode's own ring sizes and static head
       if (pl.conv == CONV_COPY) set_bulk_ring(pl.prm, false);
-      else set_cvt_ring(pl.prm, true);
+      else set_cvt_ring(pl.prm, true, -1);
       pl.prm.sched_head_stages = sched_head_stages(true);
       return launch_one(pl, static_cast<cudaStream_t>(stream));
     }
