@@ -557,8 +557,14 @@ def run_ours(args, wl: W.Workload, ws: int, rank: int, local: int):
 
 def run_e2e(wl, dev, stream, alg_bytes, steps, ws):
     """Same metric through the public binding with inputs and output in pinned
-    host memory: every step copies its inputs host -> device, gathers, and
-    copies the output device -> host."""
+    host memory: every step copies all of its inputs host -> device, gathers,
+    and copies its whole output device -> host, inside the timed region.
+
+    Steps are pipelined the way a serving loop would run them: two device
+    buffer sets, input copies on one stream, the gather on the benchmark's
+    stream, output copies on a third, ordered by events. Step k + 1's input
+    copy then overlaps step k's output copy (the host link is full duplex).
+    `serial` times the same steps one after another on one stream."""
     from paged_mla_kv_cache_gb300 import binding
     h_cache = wl.cache.pin_memory()
     h_bt = wl.block_table.pin_memory()
@@ -566,42 +572,96 @@ def run_e2e(wl, dev, stream, alg_bytes, steps, ws):
     h_ss = None if wl.seq_starts is None else wl.seq_starts.pin_memory()
     h_scale = torch.tensor([wl.scale], dtype=torch.float32).pin_memory()
     h_out = torch.empty((wl.total_tokens, wl.entry_size), dtype=W.TORCH_DTYPES[wl.dst_dtype]).pin_memory()
-    d_cache = torch.empty_like(wl.cache, device=dev)
-    d_bt = torch.empty_like(wl.block_table, device=dev)
-    d_cu = torch.empty_like(wl.cu_seq_lens, device=dev)
-    d_ss = None if h_ss is None else torch.empty_like(h_ss, device=dev)
-    d_scale = torch.empty(1, dtype=torch.float32, device=dev)
-    d_out = torch.empty(h_out.shape, dtype=h_out.dtype, device=dev)
-    d_err = torch.zeros(1, dtype=torch.int32, device=dev)
-    d_ws = binding.new_workspace(dev)
-    h2d = sum(t.numel() * t.element_size() for t in (h_cache, h_bt, h_cu, h_scale) + ((h_ss,) if h_ss is not None else ()))
+    h_in = [h_cache, h_bt, h_cu, h_scale] + ([h_ss] if h_ss is not None else [])
+
+    class Set:
+        def __init__(self):
+            self.inp = [torch.empty_like(t, device=dev) for t in h_in]
+            self.out = torch.empty(h_out.shape, dtype=h_out.dtype, device=dev)
+            self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+            self.ws = binding.new_workspace(dev)
+            self.copied = torch.cuda.Event()
+            self.gathered = torch.cuda.Event()
+            self.drained = torch.cuda.Event()
+
+        def gather(self, strm):
+            cache, bt, cu, scale = self.inp[:4]
+            ss = self.inp[4] if h_ss is not None else None
+            binding.gather(cache[:, :, :wl.entry_size], self.out, bt, cu, ss, scale, self.err,
+                           num_reqs=wl.num_reqs, stream=strm, workspace=self.ws)
+
+    sets = [Set(), Set()]
+    s_in = torch.cuda.Stream(dev)
+    s_out = torch.cuda.Stream(dev)
+    h2d = sum(t.numel() * t.element_size() for t in h_in)
     d2h = h_out.numel() * h_out.element_size()
 
-    def one():
-        d_cache.copy_(h_cache, non_blocking=True)
-        d_bt.copy_(h_bt, non_blocking=True)
-        d_cu.copy_(h_cu, non_blocking=True)
-        if d_ss is not None:
-            d_ss.copy_(h_ss, non_blocking=True)
-        d_scale.copy_(h_scale, non_blocking=True)
-        binding.gather(d_cache[:, :, :wl.entry_size], d_out, d_bt, d_cu, d_ss, d_scale, d_err,
-                       num_reqs=wl.num_reqs, stream=stream, workspace=d_ws)
-        h_out.copy_(d_out, non_blocking=True)
+    def pipelined_step(k):
+        b = sets[k % 2]
+        with torch.cuda.stream(s_in):
+            if k >= 2:
+                s_in.wait_event(b.gathered)  # step k - 2 no longer reads this set's inputs
+            for d, h in zip(b.inp, h_in):
+                d.copy_(h, non_blocking=True)
+            b.copied.record(s_in)
+        stream.wait_event(b.copied)
+        if k >= 2:
+            stream.wait_event(b.drained)  # step k - 2's output has left this set's buffer
+        b.gather(stream)
+        b.gathered.record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(b.gathered)
+            h_out.copy_(b.out, non_blocking=True)
+            b.drained.record(s_out)
 
-    for _ in range(2):
-        one()
+    def serial_step():
+        b = sets[0]
+        with torch.cuda.stream(stream):
+            for d, h in zip(b.inp, h_in):
+                d.copy_(h, non_blocking=True)
+            b.gather(stream)
+            h_out.copy_(b.out, non_blocking=True)
+
+    def timed(fn):
+        torch.cuda.synchronize(dev)
+        a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s_in)
+        stream.wait_event(a)
+        s_out.wait_event(a)
+        fn()
+        # the end event follows every stream's last operation
+        for st in (s_in, s_out):
+            ev = torch.cuda.Event()
+            ev.record(st)
+            stream.wait_event(ev)
+        e.record(stream)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(e) / steps
+
+    def run_pipelined():
+        for k in range(steps):
+            pipelined_step(k)
+
+    def run_serial():
+        for _ in range(steps):
+            serial_step()
+
+    for k in range(4):
+        pipelined_step(k)
+    serial_step()
     torch.cuda.synchronize(dev)
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(steps):
-        one()
-    b.record(stream)
-    torch.cuda.synchronize(dev)
-    ms = a.elapsed_time(b) / steps
-    if int(d_err.item()) != 0:
-        raise RuntimeError("e2e: gather reported data errors on valid inputs")
+    ms = timed(run_pipelined)
+    ms_serial = timed(run_serial)
+    for b in sets:
+        if int(b.err.item()) != 0:
+            raise RuntimeError("e2e: gather reported data errors on valid inputs")
     return {"value": round(ws * alg_bytes / (ms * 1e-3) / 1e9, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4), "steps": steps}
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4), "steps": steps,
+            "how": "pinned host buffers; two device buffer sets; input copies, gather and output copies on "
+                   "three streams ordered by events, so step k + 1's input copy overlaps step k's output copy",
+            "serial": {"value": round(ws * alg_bytes / (ms_serial * 1e-3) / 1e9, 1),
+                       "ms_per_step": round(ms_serial, 4),
+                       "how": "the same steps one after another on one stream"}}
 
 
 def sample_call(wl: W.Workload, rows: int):
