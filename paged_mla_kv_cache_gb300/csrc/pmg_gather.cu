@@ -2214,20 +2214,23 @@ int sched_head_stages(bool token_mode) {
 // launch's CTAs start in blockIdx order as the previous grid's CTAs leave (the
 // last eighth about 5 us after the first in steady state), and the late ones
 // pay their start-up (plan, block-table and first data round trips) while the
-// others already stream. The converting kernel takes a cubic tilt of 10%
-// (shares about 1.1 of even for most CTAs, falling to 0.6 for the last):
-// skew-8 0.821 -> 0.870 and 0.832 -> 0.876 of the copy peak on two boxes, one
-// fp8 request of 45,657 tokens 0.910 -> 0.937; linear tilts of 20-30% reached
-// 0.864. The byte-copy kernel keeps even shares (a tilt cost its static splits
-// 1-3.5%). PMG_SCHED_TILT_PCT (0..100) and PMG_SCHED_TILT_POW (1..4) override
-// both kernels for tuning sweeps.
+// others already stream. The converting kernel takes a quartic tilt of 8%
+// (shares 1.08 of even for most CTAs, falling to 0.68 for the last): skew-8
+// 0.871 -> 0.892 of the copy peak with its two-stage ring (0.821 -> 0.870 with
+// three 16 KB stages), one fp8 request of 45,657 tokens 0.910 -> 0.939; cubic
+// 10% and quartic 6% measured within 0.3% of it, linear 20-30% lower. A call
+// whose CTAs all start at once gains nothing from it: skew-8 after an L2 flush
+// that leaves clean lines takes about 1.7 us longer on average (the page's
+// write flush: no change). The byte-copy kernel keeps even shares (a tilt cost
+// its static splits 1-3.5%). PMG_SCHED_TILT_PCT (0..100) and
+// PMG_SCHED_TILT_POW (1..4) override both kernels for tuning sweeps.
 int sched_tilt_pct(bool converter) {
   static const int v = env_int("PMG_SCHED_TILT_PCT", -1, -1, 100);
   if (v >= 0) return v;
-  return converter ? 10 : 0;
+  return converter ? 8 : 0;
 }
 int sched_tilt_pow() {
-  static const int v = env_int("PMG_SCHED_TILT_POW", 3, 1, 4);
+  static const int v = env_int("PMG_SCHED_TILT_POW", 4, 1, 4);
   return v;
 }
 
