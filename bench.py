@@ -250,14 +250,22 @@ def kernel_of(path: str, wl: W.Workload, entry: str) -> str:
 class DeviceInputs:
     """One replica of a workload's inputs and output, resident on the device."""
 
-    def __init__(self, wl: W.Workload, device, cache=None):
+    def __init__(self, wl: W.Workload, device, cache=None, dst_offset: int = 0):
         self.cache_full = wl.cache.to(device) if cache is None else cache
         self.cache = self.cache_full[:, :, :wl.entry_size]
         self.bt = wl.block_table.to(device)
         self.cu = wl.cu_seq_lens.to(device)
         self.ss = None if wl.seq_starts is None else wl.seq_starts.to(device)
         self.scale = torch.tensor([wl.scale], dtype=torch.float32, device=device)
-        self.dst = torch.empty((wl.total_tokens, wl.entry_size), dtype=W.TORCH_DTYPES[wl.dst_dtype], device=device)
+        # dst_offset > 0: the output is rows [dst_offset, dst_offset + T) of a
+        # larger workspace, as one rank's slice before a context-parallel
+        # all-gather; rows below it are filled with a sentinel and must stay so
+        self.dst_full = torch.empty((dst_offset + wl.total_tokens, wl.entry_size),
+                                    dtype=W.TORCH_DTYPES[wl.dst_dtype], device=device)
+        if dst_offset > 0:
+            self.dst_full[:dst_offset].view(torch.uint8).fill_(0x5A)
+        self.dst = self.dst_full[dst_offset:]
+        self.dst_offset = dst_offset
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
 
     def nbytes(self):
@@ -267,13 +275,13 @@ class DeviceInputs:
 class Runner:
     """A workload on the device: replicas, one scheduling workspace, the call."""
 
-    def __init__(self, wl: W.Workload, dev, stream, args):
+    def __init__(self, wl: W.Workload, dev, stream, args, dst_offset: int = 0):
         from paged_mla_kv_cache_gb300 import binding
         self.binding = binding
         self.wl, self.dev, self.stream, self.args = wl, dev, stream, args
-        base = DeviceInputs(wl, dev)
+        base = DeviceInputs(wl, dev, dst_offset=dst_offset)
         self.nrep = max(2, math.ceil(4 * L2_BYTES / base.nbytes()))
-        self.reps = [base] + [DeviceInputs(wl, dev) for _ in range(self.nrep - 1)]
+        self.reps = [base] + [DeviceInputs(wl, dev, dst_offset=dst_offset) for _ in range(self.nrep - 1)]
         self.ws_buf = None if args.no_workspace else binding.new_workspace(dev)
         if args.entry == "tokens":
             # the per-token entry point: each output row names its request
@@ -377,6 +385,8 @@ class Runner:
             flag = int(r.err.item())
             if flag != 0:
                 raise RuntimeError(f"{self.wl.name}: gather reported data errors (flag {flag}) on valid inputs")
+            if r.dst_offset > 0 and not bool((r.dst_full[:r.dst_offset].view(torch.uint8) == 0x5A).all()):
+                raise RuntimeError(f"{self.wl.name}: rows below the output offset were written")
 
     def close(self):
         del self.reps
@@ -429,6 +439,29 @@ def run_per_config(args, dev, stream, world, headline=None):
                      "cold": cold, "cold_clean": cold_clean}
         r.close()
         del wl
+    # the 300K gather as one rank's slice of a context-parallel workspace:
+    # rows [T, 2T) of 2T rows (rank 1 of 2), replayed from CUDA graphs like
+    # every steady-state figure here
+    wl = make_workload("300k")
+    T = wl.total_tokens
+    r = Runner(wl, dev, stream, args, dst_offset=T)
+    for k in range(max(args.warmup, 3)):
+        r.step(k)
+    torch.cuda.synchronize(dev)
+    alg = wl.algorithmic_bytes()
+    n = 200
+    regions = steady(r, n, world, max_repeats=5, min_total_ms=0.0)
+    ms = statistics.median(regions) / n
+    r.check_flags()
+    out["300k_cp_slice"] = {"workload": wl.name + ", written at rows [T, 2T) of a 2T-row workspace",
+                            "bytes_per_step": alg, "dtype": dtype_label(wl), "path": r.path, "kernel": r.kernel,
+                            "dst_offset_rows": T,
+                            "steady": {"gbs": round(alg / (ms * 1e-3) / 1e9, 1),
+                                       "frac": round(alg / (ms * 1e-3) / 1e9 / peak, 4),
+                                       "per_launch_us": round(ms * 1e3, 2), "steps_per_region": n,
+                                       "regions": len(regions)},
+                            "rows_below_offset": "sentinel intact after every replica's steps"}
+    r.close()
     return out
 
 
