@@ -501,3 +501,33 @@ def test_fp32_1m_named_workload_with_workspace():
     """The 1M-token fp32 raw copy the benchmark times (2304-byte entries, output
     offsets past 2^31 bytes), in the benchmark's launch configuration."""
     _check(W.CONFIGS["fp32_1m"](), workspace=True)
+
+
+# --- the converting kernel's ring, chosen at launch from the rows each CTA
+# will hold (T / (4 x SMs)): two stages up to 128 rows per CTA, else three over
+# back-to-back or padded rows; cases on both sides of the boundary -----------
+
+def _rows_per_cta(T):
+    return T // (4 * torch.cuda.get_device_properties(0).multi_processor_count)
+
+
+@pytest.mark.parametrize("rows_per_cta,src,dst,row_stride", [
+    (120, "fp8_e4m3", "bf16", None),   # two stages
+    (128, "fp8_e4m3", "fp16", None),   # the boundary: two stages
+    (129, "fp8_e4m3", "bf16", None),   # three stages, back-to-back rows
+    (200, "fp8_e4m3", "fp32", None),
+    (140, "bf16", "fp32", None),
+    (129, "fp8_e4m3", "bf16", 640),    # three stages, padded rows
+    (100, "fp16", "fp32", 640),
+])
+@pytest.mark.parametrize("workspace", [False, True])
+def test_converter_ring_across_launch_sizes(rows_per_cta, src, dst, row_stride, workspace):
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    T = rows_per_cta * 4 * sms + 3
+    assert _rows_per_cta(T) == rows_per_cta
+    # three requests with unaligned starts: partial first and last pages
+    lens = [T // 2, 1, T - T // 2 - 1]
+    wl = W.make_workload(f"ring at {rows_per_cta} rows per CTA", lens, [37, 0, 63], 64, 576, None, src, dst, 0.05,
+                         9100 + rows_per_cta, row_stride=row_stride)
+    case = _check(wl, workspace=workspace)
+    assert binding.select_path(case.cache, case.dst, case.block_table, case.cu)[0] == "bulk"
