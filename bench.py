@@ -68,6 +68,10 @@ PROFILE_FILES = {
     "skew8": "gather_tma_convert_skew8.md",
     "skew64_raw": "gather_bulk_skew64_raw.md",
     "skew64_dequant": "gather_tma_convert_skew64_dequant.md",
+    "fp32_1m": "gather_bulk_fp32_1m.md",
+    # the per-token entry point (--entry tokens) on the same kernels in token mode
+    "tokens_skew8": "gather_tma_convert_tokens_skew8.md",
+    "tokens_60k": "gather_bulk_tokens_single60k.md",
 }
 KERNEL_SRC = os.path.join(ROOT, "paged_mla_kv_cache_gb300", "csrc", "pmg_gather.cu")
 # how L2 is kept out of the steady-state figure; one statement for both arms
@@ -513,7 +517,9 @@ def run_ours(args, wl: W.Workload, ws: int, rank: int, local: int):
     cold_clean = None if args.quick else runner.cold(read_back=True)
     peak, peak_kind = measured_peak()
     achieved = alg_bytes / (per_launch_ms * 1e-3) / 1e9
-    tr_h = profiled_traffic(args.config) if args.entry == "gather" and args.options == 0 else None
+    # the committed capture of this entry point on this workload, default options only
+    profile_key = args.config if args.entry == "gather" else f"tokens_{args.config}"
+    tr_h = profiled_traffic(profile_key) if args.options == 0 else None
     headline_entry = {"workload": wl.name, "bytes_per_step": alg_bytes, "dtype": dtype_label(wl),
                       "path": runner.path, "kernel": runner.kernel,
                       "dram_traffic_per_launch": None if tr_h is None else {"read": tr_h["read"], "write": tr_h["write"],
@@ -535,7 +541,7 @@ def run_ours(args, wl: W.Workload, ws: int, rank: int, local: int):
     if not args.quick:
         e2e = run_e2e(wl, dev, stream, alg_bytes, steps=20, ws=ws)
 
-    traffic = profiled_traffic(args.config) if args.entry == "gather" and args.options == 0 else None
+    traffic = tr_h
     result = {
         "metric": METRIC,
         "value": round(value, 1),
