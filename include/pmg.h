@@ -102,7 +102,11 @@ typedef enum pmg_path {
   PMG_PATH_BULK = 1,   /* TMA 1-D bulk loads of 16-B aligned source rows into a shared ring; byte copies
                           leave by bulk stores, converting gathers by 16-byte stores of converter warps */
   PMG_PATH_VECTOR = 2, /* SIMT loads/stores of several elements per thread */
-  PMG_PATH_SCALAR = 3  /* SIMT, one element per access (any alignment) */
+  PMG_PATH_SCALAR = 3, /* SIMT, one element per access (any alignment) */
+  PMG_PATH_REALIGN = 4 /* byte copies whose rows are not 16-B aligned (and at least 16 B long): each
+                          16-B-aligned word of a destination row is assembled from the aligned
+                          16-B source words holding its bytes; whole words by 16-B stores, the
+                          partial first and last words of a row byte by byte */
 } pmg_path;
 
 /*
@@ -269,7 +273,7 @@ int pmg_gather_tokens(const void* cache, int64_t cache_block_stride, int64_t cac
  * way pmg_gather_ex does and reports the path and the elements moved per
  * access it would use. Makes no CUDA call. Pointers are only inspected for
  * alignment and NULL. *path_out receives a pmg_path, *unit_elems_out the
- * elements per access (0 for PMG_PATH_NONE, 0 for PMG_PATH_BULK).
+ * elements per access (0 for PMG_PATH_NONE, PMG_PATH_BULK and PMG_PATH_REALIGN).
  */
 int pmg_select_path(const void* cache, int64_t cache_block_stride, int64_t cache_token_stride,
                     int64_t num_blocks, const int32_t* block_table, int64_t block_table_stride,

@@ -40,7 +40,7 @@ OPT_FORCE_SCALAR = 2
 OPT_IMPLIED_END = 4
 OPT_EARLY_METADATA = 8
 
-PATH_NAMES = {0: "none", 1: "bulk", 2: "vector", 3: "scalar"}
+PATH_NAMES = {0: "none", 1: "bulk", 2: "vector", 3: "scalar", 4: "realign"}
 WORKSPACE_INTS = 4
 MAX_REQS_PLAN = 4096       # requests one launch plans; more need a workspace
 MAX_REQS = 1 << 20         # requests one call accepts

@@ -1660,6 +1660,85 @@ __device__ __forceinline__ void convert_unit(const Raw<N * ConvTraits<CONV>::es>
   }
 }
 
+// Bytes [d, d + 16) of the 32 bytes (a, b), d in 0..15 (little-endian words).
+__device__ __forceinline__ uint4 bytes_from(const uint4& a, const uint4& b, uint32_t d) {
+  const uint32_t sh = (d & 3u) * 8u;
+  uint32_t c0, c1, c2, c3, c4;
+  switch (d >> 2) {
+    case 0: c0 = a.x; c1 = a.y; c2 = a.z; c3 = a.w; c4 = b.x; break;
+    case 1: c0 = a.y; c1 = a.z; c2 = a.w; c3 = b.x; c4 = b.y; break;
+    case 2: c0 = a.z; c1 = a.w; c2 = b.x; c3 = b.y; c4 = b.z; break;
+    default: c0 = a.w; c1 = b.x; c2 = b.y; c3 = b.z; c4 = b.w; break;
+  }
+  return make_uint4(__funnelshift_r(c0, c1, sh), __funnelshift_r(c1, c2, sh), __funnelshift_r(c2, c3, sh),
+                    __funnelshift_r(c3, c4, sh));
+}
+
+// Realigning byte copy of a segment table (the SIMT kernel with N = 0): unit
+// (row, j) is the j-th 16-byte-aligned word of the destination row, of
+// `words` per row (enough for any alignment of the row start). The word's
+// bytes of the row come from at most two aligned 16-byte source words; only
+// those holding bytes of the row are read. Whole words leave with one 16-byte
+// store; the partial first and last words of a row are written byte by byte,
+// so no byte outside the row is written.
+__device__ __forceinline__ void realign_units(const Params& p, const Segment* segs, const int64_t* unit_prefix,
+                                              int64_t total, uint32_t words) {
+  const int32_t rb = p.row_src_bytes;
+  int cur = 0;
+  for (int64_t g0 = threadIdx.x; g0 < total; g0 += static_cast<int64_t>(kUnroll) * kPlanThreads) {
+    uint4 lo[kUnroll], hi[kUnroll];
+    uint8_t* wd[kUnroll];
+    uint32_t b0[kUnroll], b1[kUnroll], dl[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t g = g0 + static_cast<int64_t>(u) * kPlanThreads;
+      wd[u] = nullptr;
+      b0[u] = b1[u] = dl[u] = 0;
+      lo[u] = hi[u] = make_uint4(0u, 0u, 0u, 0u);
+      if (g < total) {
+        while (unit_prefix[cur + 1] <= g) ++cur;
+        const Segment& sg = segs[cur];
+        const uint32_t local = static_cast<uint32_t>(g - unit_prefix[cur]);
+        const uint32_t row = fast_div(local, p.upr_magic, p.upr_shift);
+        const uint32_t j = local - row * words;
+        const uint8_t* src = p.cache + sg.src + static_cast<int64_t>(row) * p.tok_stride_b;
+        uint8_t* dst = p.dst + sg.dst + static_cast<int64_t>(row) * p.dst_stride_b;
+        const int32_t mis = static_cast<int32_t>(reinterpret_cast<uintptr_t>(dst) & 15u);
+        // the word holds row bytes [w0, w0 + 16) (w0 < 0 for the first word)
+        const int32_t w0 = 16 * static_cast<int32_t>(j) - mis;
+        const int32_t first = w0 > 0 ? w0 : 0;
+        const int32_t end = w0 + 16 < rb ? w0 + 16 : rb;
+        if (first < end) {
+          const uintptr_t s0 = reinterpret_cast<uintptr_t>(src);
+          const uintptr_t a = s0 + static_cast<uintptr_t>(static_cast<intptr_t>(w0));  // source of row byte w0
+          const uintptr_t base = a & ~static_cast<uintptr_t>(15);
+          if (s0 + static_cast<uintptr_t>(first) < base + 16u)
+            lo[u] = __ldcs(reinterpret_cast<const uint4*>(base));
+          if (s0 + static_cast<uintptr_t>(end - 1) >= base + 16u)
+            hi[u] = __ldcs(reinterpret_cast<const uint4*>(base + 16u));
+          wd[u] = dst - mis + 16 * static_cast<int64_t>(j);
+          b0[u] = static_cast<uint32_t>(first - w0);
+          b1[u] = static_cast<uint32_t>(end - w0);
+          dl[u] = static_cast<uint32_t>(a - base);
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      if (wd[u] == nullptr) continue;
+      const uint4 w = bytes_from(lo[u], hi[u], dl[u]);
+      if (b0[u] == 0 && b1[u] == 16) {
+        *reinterpret_cast<uint4*>(wd[u]) = w;
+      } else {
+        for (uint32_t k = b0[u]; k < b1[u]; ++k) {
+          const uint32_t x = k < 4 ? w.x : (k < 8 ? w.y : (k < 12 ? w.z : w.w));
+          wd[u][k] = static_cast<uint8_t>(x >> (8u * (k & 3u)));
+        }
+      }
+    }
+  }
+}
+
 template <int CONV, int N>
 __global__ void __launch_bounds__(kPlanThreads) gather_simt_kernel(const __grid_constant__ Params p) {
   constexpr int kInBytes = N * ConvTraits<CONV>::es;
@@ -1716,6 +1795,9 @@ __global__ void __launch_bounds__(kPlanThreads) gather_simt_kernel(const __grid_
 
     const int64_t total = unit_prefix[kPlanThreads];
     int cur = 0;
+    if constexpr (N == 0) {
+      realign_units(p, segs, unit_prefix, total, upr);
+    } else {
     for (int64_t g0 = tid; g0 < total; g0 += static_cast<int64_t>(kUnroll) * kPlanThreads) {
       Raw<kInBytes> in[kUnroll];
       uint8_t* dptr[kUnroll];
@@ -1749,6 +1831,7 @@ __global__ void __launch_bounds__(kPlanThreads) gather_simt_kernel(const __grid_
           store_raw<kOutBytes>(dptr[u], out);
         }
       }
+    }
     }
     const bool last = nseg < kPlanThreads;
     __syncthreads();
@@ -2182,6 +2265,13 @@ int prefetch_stages() {
   return v;
 }
 
+// The realigning byte copy for rows that are not 16-byte aligned
+// (PMG_REALIGN=0 keeps them on the narrow-unit SIMT kernels, for A/B runs).
+bool use_realign() {
+  static const int v = env_int("PMG_REALIGN", 1, 0, 1);
+  return v != 0;
+}
+
 // Speculative start of the TMA paths (PMG_SPEC=0 turns it off).
 bool use_spec() {
   static const int v = env_int("PMG_SPEC", 1, 0, 1);
@@ -2406,6 +2496,13 @@ int make_plan(const void* cache, int64_t cbs, int64_t cts, int64_t num_blocks, c
       set_cvt_ring(q, false, -1);  // sized again at launch, from the grid
       q.sched_tilt_pct = sched_tilt_pct(true);
       q.dense = q.dst_dense;
+    } else if (conv == CONV_COPY && !forced && unit < 16 && q.row_src_bytes >= 16 && use_realign()) {
+      // rows not 16-byte aligned: whole 16-byte words of each destination row,
+      // assembled from aligned source words (the SIMT kernel's N = 0 mover)
+      out.path = PMG_PATH_REALIGN;
+      out.unit = 0;
+      upr = (static_cast<int64_t>(q.row_src_bytes) + 15 + 15) / 16;
+      q.dense = 0;
     } else {
       const int64_t unit_elems = (conv == CONV_COPY) ? unit / es : unit;
       out.path = (unit_elems > 1) ? PMG_PATH_VECTOR : PMG_PATH_SCALAR;
@@ -2441,7 +2538,7 @@ KernelFn simt_kernel_for(int conv, int unit) {
 #define PMG_CASE(C, N) \
   if (conv == C && unit == N) return gather_simt_kernel<C, N>;
   PMG_CASE(CONV_COPY, 16) PMG_CASE(CONV_COPY, 8) PMG_CASE(CONV_COPY, 4) PMG_CASE(CONV_COPY, 2)
-  PMG_CASE(CONV_COPY, 1)
+  PMG_CASE(CONV_COPY, 1) PMG_CASE(CONV_COPY, 0)
   PMG_CASE(CONV_E4M3_BF16, 16) PMG_CASE(CONV_E4M3_BF16, 4) PMG_CASE(CONV_E4M3_BF16, 1)
   PMG_CASE(CONV_E4M3_F16, 16) PMG_CASE(CONV_E4M3_F16, 4) PMG_CASE(CONV_E4M3_F16, 1)
   PMG_CASE(CONV_E4M3_F32, 16) PMG_CASE(CONV_E4M3_F32, 4) PMG_CASE(CONV_E4M3_F32, 1)
@@ -2474,7 +2571,7 @@ const KernelFn kAllSimt[] = {
     gather_simt_kernel<CONV_E4M3_F16, 4>,   gather_simt_kernel<CONV_E4M3_F16, 1>,  gather_simt_kernel<CONV_E4M3_F32, 16>,
     gather_simt_kernel<CONV_E4M3_F32, 4>,   gather_simt_kernel<CONV_E4M3_F32, 1>,  gather_simt_kernel<CONV_BF16_F32, 8>,
     gather_simt_kernel<CONV_BF16_F32, 2>,   gather_simt_kernel<CONV_BF16_F32, 1>,  gather_simt_kernel<CONV_F16_F32, 8>,
-    gather_simt_kernel<CONV_F16_F32, 2>,    gather_simt_kernel<CONV_F16_F32, 1>,
+    gather_simt_kernel<CONV_F16_F32, 2>,    gather_simt_kernel<CONV_F16_F32, 1>,  gather_simt_kernel<CONV_COPY, 0>,
 };
 
 KernelFn tma_convert_kernel_for(int conv) {

@@ -96,7 +96,11 @@ def test_nothing_to_do_launches_nothing(cuda_lib, over):
     (dict(opt=binding.OPT_FORCE_SIMT), "vector", 8),                      # 16 B = 8 bf16
     (dict(opt=binding.OPT_FORCE_SCALAR), "scalar", 1),
     (dict(cts=640, cbs=64 * 640), "bulk", 0),                             # padded rows, still 16-B aligned
-    (dict(cts=577, cbs=64 * 577), "scalar", 1),                           # 1154-B row starts: one bf16 per access
+    (dict(cts=577, cbs=64 * 577), "realign", 0),                          # 1154-B row starts: realigned 16-B words
+    (dict(cts=577, cbs=64 * 577, opt=binding.OPT_FORCE_SIMT), "scalar", 1),  # forced SIMT: one bf16 per access
+    (dict(cts=580, cbs=64 * 580), "realign", 0),                          # 8-B aligned rows: realigned too
+    (dict(cts=580, cbs=64 * 580, opt=binding.OPT_FORCE_SIMT), "vector", 4),
+    (dict(dts=577), "realign", 0),                                        # only the output rows unaligned
     (dict(E=7, cts=7, cbs=64 * 7, dts=7), "scalar", 1),
     (dict(sdt=3, ddt=0), "bulk", 0),                                      # fp8 -> bf16: TMA in, converter warps out
     (dict(sdt=3, ddt=0, opt=binding.OPT_FORCE_SIMT), "vector", 16),       # fp8 -> bf16 SIMT, 16 codes per load
@@ -110,6 +114,8 @@ def test_nothing_to_do_launches_nothing(cuda_lib, over):
     (dict(sdt=2, ddt=2), "bulk", 0),                                      # fp32 copy
     (dict(sdt=4, ddt=4, E=5, cts=5, cbs=320, dts=5), "scalar", 1),       # u8 odd rows
     (dict(sdt=4, ddt=4, E=12, cts=12, cbs=768, dts=12), "vector", 4),     # u8 rows of 12 B: 4-byte units
+    (dict(sdt=4, ddt=4, E=17, cts=17, cbs=64 * 17, dts=17), "realign", 0),  # u8 rows of 17 B
+    (dict(sdt=2, ddt=2, E=5, cts=5, cbs=320, dts=5), "realign", 0),       # fp32 rows of 20 B
 ])
 def test_path_selection(cuda_lib, over, path, unit):
     st, p, u = _path(cuda_lib, _args(**over))

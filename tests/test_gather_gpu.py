@@ -20,7 +20,7 @@ from oracle import plan as op
 from paged_mla_kv_cache_gb300 import binding
 from paged_mla_kv_cache_gb300 import workloads as W
 
-from gpu_helpers import DeviceCase, assert_same, oracle_run
+from gpu_helpers import GUARD_BYTES, DeviceCase, assert_same, oracle_run
 
 pytestmark = pytest.mark.gpu
 
@@ -531,3 +531,91 @@ def test_converter_ring_across_launch_sizes(rows_per_cta, src, dst, row_stride, 
                          9100 + rows_per_cta, row_stride=row_stride)
     case = _check(wl, workspace=workspace)
     assert binding.select_path(case.cache, case.dst, case.block_table, case.cu)[0] == "bulk"
+
+
+# --- the realigning byte copy: raw copies whose rows are not 16-byte aligned
+# (odd strides on either side, or a base that is not 16-byte aligned) ---------
+
+def _realign_case(seed, dtype, E, src_stride, dst_stride, src_off=0, dst_off=0, B=16, R=5):
+    rng = np.random.default_rng(seed)
+    lens = [int(x) for x in rng.integers(0, 3 * B + 5, R)]
+    lens[int(rng.integers(0, R))] = 0
+    starts = [int(x) for x in rng.integers(0, 2 * B + 1, R)]
+    assert src_off + E <= src_stride
+    wl = W.make_workload("realign", lens, starts, B, E, None, dtype, dtype, 1.0, seed, row_stride=src_stride)
+    T, ed = wl.total_tokens, W.ELEM_BYTES[dtype]
+    # oracle on the same element window of each cache row
+    cache_bits = W.tensor_bits(wl.cache)
+    view = np.lib.stride_tricks.as_strided(cache_bits[:, :, src_off:], shape=(cache_bits.shape[0], B, E),
+                                           strides=cache_bits.strides)
+    want = np.full((T, dst_stride * ed), 0xA5, np.uint8).view(W.NP_BITS[ed])
+    oflag = og.gather(view, wl.block_table.numpy(), wl.cu_seq_lens.numpy(), wl.seq_starts.numpy(), R, T, B, E,
+                      dtype, dtype, 1.0, want)
+    # device: cache window at element src_off; dst rows of dst_stride elements
+    # starting dst_off elements into a guarded buffer
+    dev = "cuda:0"
+    full = wl.cache.to(dev)
+    cache = full[:, :, src_off:src_off + E]
+    body_elems = dst_off + T * dst_stride
+    raw = torch.full((2 * GUARD_BYTES + body_elems * ed,), 0xA5, dtype=torch.uint8, device=dev)
+    flat = raw[GUARD_BYTES:GUARD_BYTES + body_elems * ed].view(W.TORCH_DTYPES[dtype])
+    dst = flat[dst_off:].view(T, dst_stride)[:, :E]
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    path, _ = binding.select_path(cache, dst, wl.block_table.to(dev), wl.cu_seq_lens.to(dev))
+    binding.gather(cache, dst, wl.block_table.to(dev), wl.cu_seq_lens.to(dev), wl.seq_starts.to(dev),
+                   torch.tensor([1.0], device=dev), err, num_reqs=R)
+    torch.cuda.synchronize()
+    r = raw.cpu().numpy()
+    assert np.all(r[:GUARD_BYTES] == 0xA5) and np.all(r[-GUARD_BYTES:] == 0xA5), "guard regions written"
+    body = r[GUARD_BYTES:len(r) - GUARD_BYTES]
+    assert np.all(body[:dst_off * ed] == 0xA5), "bytes before the first row written"
+    got = body[dst_off * ed:].view(W.NP_BITS[ed]).reshape(T, dst_stride)
+    assert oflag == 0 and int(err.item()) == 0
+    assert_same(got, want, dtype, False)
+    return path
+
+
+@pytest.mark.parametrize("dtype,E,src_stride,dst_stride,src_off,dst_off", [
+    ("bf16", 576, 577, 576, 0, 0),     # source rows step 2 bytes off alignment per row
+    ("bf16", 576, 576, 577, 0, 0),     # destination rows do
+    ("bf16", 576, 581, 583, 0, 0),
+    ("bf16", 576, 580, 580, 0, 0),     # 8-byte aligned rows
+    ("bf16", 576, 584, 576, 1, 0),     # aligned row stride, window 2 bytes into each row
+    ("bf16", 576, 576, 576, 0, 3),     # output starts 6 bytes into the buffer
+    ("bf16", 576, 592, 584, 7, 5),
+    ("bf16", 8, 9, 11, 0, 0),          # 16-byte rows, always split over two words
+    ("u8", 17, 17, 17, 0, 0),
+    ("u8", 31, 36, 31, 3, 1),
+    ("u8", 100, 101, 103, 0, 0),
+    ("u8", 1000, 1024, 1001, 15, 13),
+    ("fp8_e4m3", 576, 577, 577, 0, 0),  # fp8 raw copy: byte rows
+    ("fp32", 5, 5, 5, 0, 0),           # 20-byte rows
+    ("fp32", 7, 9, 7, 1, 2),
+    ("fp32", 290, 290, 291, 0, 1),
+])
+def test_realigning_copy(dtype, E, src_stride, dst_stride, src_off, dst_off):
+    path = _realign_case(500 + E + src_stride + 7 * src_off + 13 * dst_off, dtype, E, src_stride, dst_stride,
+                         src_off, dst_off)
+    assert path == "realign"
+
+
+@pytest.mark.parametrize("B,R", [(64, 3), (1, 40), (128, 2)])
+def test_realigning_copy_pages_and_requests(B, R):
+    """Full pages, one-token pages and long pages, many requests."""
+    assert _realign_case(77 + B + R, "bf16", 576, 579, 577, 1, 1, B=B, R=R) == "realign"
+
+
+def test_realigning_copy_matches_forced_scalar():
+    """The realigning copy and the one-element-per-access kernel write the same
+    bytes (and the same untouched padding) on a named-size workload with odd
+    strides on both sides."""
+    wl = _small(31, "bf16", "bf16", 64, 576, row_stride=579, R=6)
+    a = DeviceCase(wl, dst_row_stride=581)
+    assert binding.select_path(a.cache, a.dst, a.block_table, a.cu)[0] == "realign"
+    a.run()
+    b = DeviceCase(wl, dst_row_stride=581)
+    b.run(options=binding.OPT_FORCE_SCALAR)
+    ga, fa, _ = a.result()
+    gb, fb, _ = b.result()
+    assert fa == fb == 0
+    assert np.array_equal(ga, gb)
