@@ -103,10 +103,13 @@ typedef enum pmg_path {
                           leave by bulk stores, converting gathers by 16-byte stores of converter warps */
   PMG_PATH_VECTOR = 2, /* SIMT loads/stores of several elements per thread */
   PMG_PATH_SCALAR = 3, /* SIMT, one element per access (any alignment) */
-  PMG_PATH_REALIGN = 4 /* byte copies whose rows are not 16-B aligned (and at least 16 B long): each
+  PMG_PATH_REALIGN = 4 /* rows of at least 16 output bytes that the TMA paths cannot take (byte
+                          copies whose rows are not 16-B aligned; converting gathers whose rows are
+                          not 16-B aligned or not a whole number of converter units): each
                           16-B-aligned word of a destination row is assembled from the aligned
-                          16-B source words holding its bytes; whole words by 16-B stores, the
-                          partial first and last words of a row byte by byte */
+                          16-B source words holding its bytes (converted for a converting gather);
+                          whole words by 16-B stores, the partial first and last words of a row
+                          byte by byte */
 } pmg_path;
 
 /*

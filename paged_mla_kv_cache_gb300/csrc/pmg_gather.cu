@@ -1739,6 +1739,83 @@ __device__ __forceinline__ void realign_units(const Params& p, const Segment* se
   }
 }
 
+// Realigning converting gather (the SIMT kernel with N = 0 and a conversion):
+// unit (row, j) is the j-th 16-byte-aligned word of the destination row,
+// 16 / ed elements starting at element e0 (negative for a row's first word
+// when the row starts inside a word). Their source bytes (at most 8) come from
+// at most two aligned 16-byte source words, read only where they hold bytes of
+// the row's elements; the elements are converted as one TMA-converter unit;
+// whole words leave with one 16-byte store, the partial first and last words
+// of a row element by element.
+template <int CONV>
+__device__ __forceinline__ void realign_convert_units(const Params& p, const Segment* segs,
+                                                      const int64_t* unit_prefix, int64_t total, uint32_t words,
+                                                      float scale) {
+  constexpr int es = ConvTraits<CONV>::es;
+  constexpr int ed = ConvTraits<CONV>::ed;
+  constexpr int n = 16 / ed;   // elements per destination word
+  constexpr int kIn = n * es;  // their source bytes
+  static_assert(kIn == 4 || kIn == 8, "source bytes per word");
+  const int32_t E = p.row_dst_bytes / ed;
+  int cur = 0;
+  for (int64_t g0 = threadIdx.x; g0 < total; g0 += static_cast<int64_t>(kUnroll) * kPlanThreads) {
+    uint4 lo[kUnroll], hi[kUnroll];
+    uint8_t* wd[kUnroll];
+    int32_t f0[kUnroll], f1[kUnroll];
+    uint32_t dl[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t g = g0 + static_cast<int64_t>(u) * kPlanThreads;
+      wd[u] = nullptr;
+      f0[u] = f1[u] = 0;
+      dl[u] = 0;
+      lo[u] = hi[u] = make_uint4(0u, 0u, 0u, 0u);
+      if (g < total) {
+        while (unit_prefix[cur + 1] <= g) ++cur;
+        const Segment& sg = segs[cur];
+        const uint32_t local = static_cast<uint32_t>(g - unit_prefix[cur]);
+        const uint32_t row = fast_div(local, p.upr_magic, p.upr_shift);
+        const uint32_t j = local - row * words;
+        const uint8_t* src = p.cache + sg.src + static_cast<int64_t>(row) * p.tok_stride_b;
+        uint8_t* dst = p.dst + sg.dst + static_cast<int64_t>(row) * p.dst_stride_b;
+        const int32_t mis = static_cast<int32_t>(reinterpret_cast<uintptr_t>(dst) & 15u);  // a multiple of ed
+        const int32_t e0 = (16 * static_cast<int32_t>(j) - mis) / ed;
+        const int32_t first = e0 > 0 ? e0 : 0;
+        const int32_t end = e0 + n < E ? e0 + n : E;
+        if (first < end) {
+          const uintptr_t s0 = reinterpret_cast<uintptr_t>(src);
+          const uintptr_t a = s0 + static_cast<uintptr_t>(static_cast<intptr_t>(e0) * es);  // element e0's source
+          const uintptr_t base = a & ~static_cast<uintptr_t>(15);
+          if (s0 + static_cast<uintptr_t>(first * es) < base + 16u)
+            lo[u] = __ldcs(reinterpret_cast<const uint4*>(base));
+          if (s0 + static_cast<uintptr_t>(end * es - 1) >= base + 16u)
+            hi[u] = __ldcs(reinterpret_cast<const uint4*>(base + 16u));
+          wd[u] = dst - mis + 16 * static_cast<int64_t>(j);
+          f0[u] = first - e0;
+          f1[u] = end - e0;
+          dl[u] = static_cast<uint32_t>(a - base);
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      if (wd[u] == nullptr) continue;
+      const uint4 w = bytes_from(lo[u], hi[u], dl[u]);
+      Raw<kIn> in;
+      in.w[0] = w.x;
+      if constexpr (kIn == 8) in.w[1] = w.y;
+      Raw<16> out;
+      convert_unit<CONV, n>(in, out, scale);
+      if (f0[u] == 0 && f1[u] == n) {
+        store_raw<16>(wd[u], out);
+      } else {
+        for (int32_t k = f0[u] * ed; k < f1[u] * ed; ++k)
+          wd[u][k] = static_cast<uint8_t>(out.w[k >> 2] >> (8 * (k & 3)));
+      }
+    }
+  }
+}
+
 template <int CONV, int N>
 __global__ void __launch_bounds__(kPlanThreads) gather_simt_kernel(const __grid_constant__ Params p) {
   constexpr int kInBytes = N * ConvTraits<CONV>::es;
@@ -1795,8 +1872,10 @@ __global__ void __launch_bounds__(kPlanThreads) gather_simt_kernel(const __grid_
 
     const int64_t total = unit_prefix[kPlanThreads];
     int cur = 0;
-    if constexpr (N == 0) {
+    if constexpr (N == 0 && CONV == CONV_COPY) {
       realign_units(p, segs, unit_prefix, total, upr);
+    } else if constexpr (N == 0) {
+      realign_convert_units<CONV>(p, segs, unit_prefix, total, upr, scale);
     } else {
     for (int64_t g0 = tid; g0 < total; g0 += static_cast<int64_t>(kUnroll) * kPlanThreads) {
       Raw<kInBytes> in[kUnroll];
@@ -2496,12 +2575,15 @@ int make_plan(const void* cache, int64_t cbs, int64_t cts, int64_t num_blocks, c
       set_cvt_ring(q, false, -1);  // sized again at launch, from the grid
       q.sched_tilt_pct = sched_tilt_pct(true);
       q.dense = q.dst_dense;
-    } else if (conv == CONV_COPY && !forced && unit < 16 && q.row_src_bytes >= 16 && use_realign()) {
-      // rows not 16-byte aligned: whole 16-byte words of each destination row,
-      // assembled from aligned source words (the SIMT kernel's N = 0 mover)
+    } else if (!forced && q.row_dst_bytes >= 16 && use_realign() &&
+               (conv == CONV_COPY ? unit < 16 : cu_unit > 0)) {
+      // rows not 16-byte aligned (or converting rows whose length is not a
+      // whole number of converter units): whole 16-byte words of each
+      // destination row, assembled from aligned source words (the SIMT
+      // kernel's N = 0 movers)
       out.path = PMG_PATH_REALIGN;
       out.unit = 0;
-      upr = (static_cast<int64_t>(q.row_src_bytes) + 15 + 15) / 16;
+      upr = (static_cast<int64_t>(q.row_dst_bytes) + 15 + 15) / 16;
       q.dense = 0;
     } else {
       const int64_t unit_elems = (conv == CONV_COPY) ? unit / es : unit;
@@ -2539,11 +2621,11 @@ KernelFn simt_kernel_for(int conv, int unit) {
   if (conv == C && unit == N) return gather_simt_kernel<C, N>;
   PMG_CASE(CONV_COPY, 16) PMG_CASE(CONV_COPY, 8) PMG_CASE(CONV_COPY, 4) PMG_CASE(CONV_COPY, 2)
   PMG_CASE(CONV_COPY, 1) PMG_CASE(CONV_COPY, 0)
-  PMG_CASE(CONV_E4M3_BF16, 16) PMG_CASE(CONV_E4M3_BF16, 4) PMG_CASE(CONV_E4M3_BF16, 1)
-  PMG_CASE(CONV_E4M3_F16, 16) PMG_CASE(CONV_E4M3_F16, 4) PMG_CASE(CONV_E4M3_F16, 1)
-  PMG_CASE(CONV_E4M3_F32, 16) PMG_CASE(CONV_E4M3_F32, 4) PMG_CASE(CONV_E4M3_F32, 1)
-  PMG_CASE(CONV_BF16_F32, 8) PMG_CASE(CONV_BF16_F32, 2) PMG_CASE(CONV_BF16_F32, 1)
-  PMG_CASE(CONV_F16_F32, 8) PMG_CASE(CONV_F16_F32, 2) PMG_CASE(CONV_F16_F32, 1)
+  PMG_CASE(CONV_E4M3_BF16, 16) PMG_CASE(CONV_E4M3_BF16, 4) PMG_CASE(CONV_E4M3_BF16, 1) PMG_CASE(CONV_E4M3_BF16, 0)
+  PMG_CASE(CONV_E4M3_F16, 16) PMG_CASE(CONV_E4M3_F16, 4) PMG_CASE(CONV_E4M3_F16, 1) PMG_CASE(CONV_E4M3_F16, 0)
+  PMG_CASE(CONV_E4M3_F32, 16) PMG_CASE(CONV_E4M3_F32, 4) PMG_CASE(CONV_E4M3_F32, 1) PMG_CASE(CONV_E4M3_F32, 0)
+  PMG_CASE(CONV_BF16_F32, 8) PMG_CASE(CONV_BF16_F32, 2) PMG_CASE(CONV_BF16_F32, 1) PMG_CASE(CONV_BF16_F32, 0)
+  PMG_CASE(CONV_F16_F32, 8) PMG_CASE(CONV_F16_F32, 2) PMG_CASE(CONV_F16_F32, 1) PMG_CASE(CONV_F16_F32, 0)
 #undef PMG_CASE
   return nullptr;
 }
@@ -2572,6 +2654,8 @@ const KernelFn kAllSimt[] = {
     gather_simt_kernel<CONV_E4M3_F32, 4>,   gather_simt_kernel<CONV_E4M3_F32, 1>,  gather_simt_kernel<CONV_BF16_F32, 8>,
     gather_simt_kernel<CONV_BF16_F32, 2>,   gather_simt_kernel<CONV_BF16_F32, 1>,  gather_simt_kernel<CONV_F16_F32, 8>,
     gather_simt_kernel<CONV_F16_F32, 2>,    gather_simt_kernel<CONV_F16_F32, 1>,  gather_simt_kernel<CONV_COPY, 0>,
+    gather_simt_kernel<CONV_E4M3_BF16, 0>,  gather_simt_kernel<CONV_E4M3_F16, 0>,  gather_simt_kernel<CONV_E4M3_F32, 0>,
+    gather_simt_kernel<CONV_BF16_F32, 0>,   gather_simt_kernel<CONV_F16_F32, 0>,
 };
 
 KernelFn tma_convert_kernel_for(int conv) {

@@ -104,13 +104,18 @@ def test_nothing_to_do_launches_nothing(cuda_lib, over):
     (dict(E=7, cts=7, cbs=64 * 7, dts=7), "scalar", 1),
     (dict(sdt=3, ddt=0), "bulk", 0),                                      # fp8 -> bf16: TMA in, converter warps out
     (dict(sdt=3, ddt=0, opt=binding.OPT_FORCE_SIMT), "vector", 16),       # fp8 -> bf16 SIMT, 16 codes per load
-    (dict(sdt=3, ddt=0, cts=577, cbs=64 * 577), "scalar", 1),
+    (dict(sdt=3, ddt=0, cts=577, cbs=64 * 577), "realign", 0),           # odd fp8 rows: realigned words
+    (dict(sdt=3, ddt=0, cts=577, cbs=64 * 577, opt=binding.OPT_FORCE_SIMT), "scalar", 1),
     (dict(sdt=3, ddt=0, cts=640, cbs=64 * 640, dts=600), "bulk", 0),      # padded rows on both sides
-    (dict(sdt=3, ddt=0, E=572, cts=572, cbs=64 * 572, dts=572), "vector", 4),  # 572 % 8 != 0: SIMT
+    (dict(sdt=3, ddt=0, E=572, cts=572, cbs=64 * 572, dts=572), "realign", 0),  # 572 % 8 != 0: no TMA units
+    (dict(sdt=3, ddt=0, E=572, cts=572, cbs=64 * 572, dts=572, opt=binding.OPT_FORCE_SIMT), "vector", 4),
     (dict(sdt=3, ddt=2, dst=32 * 1024 + 16), "bulk", 0),                  # fp32 out, 16-B aligned
-    (dict(sdt=3, ddt=2, dst=32 * 1024 + 4), "scalar", 1),                 # fp32 out, only 4-B aligned rows
+    (dict(sdt=3, ddt=2, dst=32 * 1024 + 4), "realign", 0),                # fp32 out, only 4-B aligned rows
+    (dict(sdt=3, ddt=2, dst=32 * 1024 + 4, opt=binding.OPT_FORCE_SIMT), "scalar", 1),
     (dict(sdt=0, ddt=2), "bulk", 0),                                      # bf16 -> fp32
-    (dict(sdt=0, ddt=2, dts=578), "vector", 2),                           # bf16 -> fp32, 8-B aligned out rows
+    (dict(sdt=0, ddt=2, dts=578), "realign", 0),                          # bf16 -> fp32, 8-B aligned out rows
+    (dict(sdt=0, ddt=2, dts=578, opt=binding.OPT_FORCE_SIMT), "vector", 2),
+    (dict(sdt=3, ddt=0, E=7, cts=7, cbs=64 * 7, dts=7), "scalar", 1),    # 14-B output rows: below one word
     (dict(sdt=2, ddt=2), "bulk", 0),                                      # fp32 copy
     (dict(sdt=4, ddt=4, E=5, cts=5, cbs=320, dts=5), "scalar", 1),       # u8 odd rows
     (dict(sdt=4, ddt=4, E=12, cts=12, cbs=768, dts=12), "vector", 4),     # u8 rows of 12 B: 4-byte units

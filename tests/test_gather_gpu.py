@@ -536,21 +536,23 @@ def test_converter_ring_across_launch_sizes(rows_per_cta, src, dst, row_stride, 
 # --- the realigning byte copy: raw copies whose rows are not 16-byte aligned
 # (odd strides on either side, or a base that is not 16-byte aligned) ---------
 
-def _realign_case(seed, dtype, E, src_stride, dst_stride, src_off=0, dst_off=0, B=16, R=5):
+def _realign_case(seed, dtype, E, src_stride, dst_stride, src_off=0, dst_off=0, B=16, R=5, out_dtype=None,
+                  scale=1.0):
+    out_dtype = out_dtype or dtype
     rng = np.random.default_rng(seed)
     lens = [int(x) for x in rng.integers(0, 3 * B + 5, R)]
     lens[int(rng.integers(0, R))] = 0
     starts = [int(x) for x in rng.integers(0, 2 * B + 1, R)]
     assert src_off + E <= src_stride
-    wl = W.make_workload("realign", lens, starts, B, E, None, dtype, dtype, 1.0, seed, row_stride=src_stride)
-    T, ed = wl.total_tokens, W.ELEM_BYTES[dtype]
+    wl = W.make_workload("realign", lens, starts, B, E, None, dtype, out_dtype, scale, seed, row_stride=src_stride)
+    T, ed = wl.total_tokens, W.ELEM_BYTES[out_dtype]
     # oracle on the same element window of each cache row
     cache_bits = W.tensor_bits(wl.cache)
     view = np.lib.stride_tricks.as_strided(cache_bits[:, :, src_off:], shape=(cache_bits.shape[0], B, E),
                                            strides=cache_bits.strides)
     want = np.full((T, dst_stride * ed), 0xA5, np.uint8).view(W.NP_BITS[ed])
     oflag = og.gather(view, wl.block_table.numpy(), wl.cu_seq_lens.numpy(), wl.seq_starts.numpy(), R, T, B, E,
-                      dtype, dtype, 1.0, want)
+                      dtype, out_dtype, scale, want)
     # device: cache window at element src_off; dst rows of dst_stride elements
     # starting dst_off elements into a guarded buffer
     dev = "cuda:0"
@@ -558,12 +560,12 @@ def _realign_case(seed, dtype, E, src_stride, dst_stride, src_off=0, dst_off=0, 
     cache = full[:, :, src_off:src_off + E]
     body_elems = dst_off + T * dst_stride
     raw = torch.full((2 * GUARD_BYTES + body_elems * ed,), 0xA5, dtype=torch.uint8, device=dev)
-    flat = raw[GUARD_BYTES:GUARD_BYTES + body_elems * ed].view(W.TORCH_DTYPES[dtype])
+    flat = raw[GUARD_BYTES:GUARD_BYTES + body_elems * ed].view(W.TORCH_DTYPES[out_dtype])
     dst = flat[dst_off:].view(T, dst_stride)[:, :E]
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     path, _ = binding.select_path(cache, dst, wl.block_table.to(dev), wl.cu_seq_lens.to(dev))
     binding.gather(cache, dst, wl.block_table.to(dev), wl.cu_seq_lens.to(dev), wl.seq_starts.to(dev),
-                   torch.tensor([1.0], device=dev), err, num_reqs=R)
+                   torch.tensor([scale], device=dev), err, num_reqs=R)
     torch.cuda.synchronize()
     r = raw.cpu().numpy()
     assert np.all(r[:GUARD_BYTES] == 0xA5) and np.all(r[-GUARD_BYTES:] == 0xA5), "guard regions written"
@@ -571,7 +573,7 @@ def _realign_case(seed, dtype, E, src_stride, dst_stride, src_off=0, dst_off=0, 
     assert np.all(body[:dst_off * ed] == 0xA5), "bytes before the first row written"
     got = body[dst_off * ed:].view(W.NP_BITS[ed]).reshape(T, dst_stride)
     assert oflag == 0 and int(err.item()) == 0
-    assert_same(got, want, dtype, False)
+    assert_same(got, want, out_dtype, out_dtype != dtype)
     return path
 
 
@@ -619,3 +621,24 @@ def test_realigning_copy_matches_forced_scalar():
     gb, fb, _ = b.result()
     assert fa == fb == 0
     assert np.array_equal(ga, gb)
+
+
+@pytest.mark.parametrize("src,dst,E,src_stride,dst_stride,src_off,dst_off", [
+    ("fp8_e4m3", "bf16", 576, 577, 576, 0, 0),   # odd source rows, aligned output rows
+    ("fp8_e4m3", "bf16", 576, 576, 577, 0, 0),   # output rows 2 bytes off per row
+    ("fp8_e4m3", "bf16", 576, 592, 576, 5, 3),   # windows off alignment on both sides
+    ("fp8_e4m3", "bf16", 572, 572, 572, 0, 0),   # aligned rows, not a whole number of converter units
+    ("fp8_e4m3", "bf16", 9, 9, 9, 0, 0),         # 18-byte output rows: two partial words
+    ("fp8_e4m3", "fp16", 576, 579, 581, 0, 0),
+    ("fp8_e4m3", "fp32", 576, 577, 577, 0, 0),
+    ("fp8_e4m3", "fp32", 5, 5, 5, 0, 1),         # 20-byte output rows
+    ("bf16", "fp32", 576, 577, 578, 0, 0),
+    ("bf16", "fp32", 8, 9, 8, 1, 0),
+    ("fp16", "fp32", 100, 101, 103, 0, 1),
+    ("fp16", "fp32", 100, 112, 100, 7, 0),
+])
+def test_realigning_converting_gather(src, dst, E, src_stride, dst_stride, src_off, dst_off):
+    scale = 0.05 if src == "fp8_e4m3" else 1.0
+    path = _realign_case(900 + E + src_stride + 7 * src_off + 13 * dst_off, src, E, src_stride, dst_stride,
+                         src_off, dst_off, out_dtype=dst, scale=scale)
+    assert path == "realign"
