@@ -49,7 +49,7 @@ def _case(seed):
     return wl, dst_stride, options, workspace
 
 
-@pytest.mark.parametrize("seed", range(150))
+@pytest.mark.parametrize("seed", range(300))
 def test_random_gather(seed):
     wl, dst_stride, options, workspace = _case(seed)
     case = DeviceCase(wl, dst_row_stride=dst_stride, workspace=workspace)
