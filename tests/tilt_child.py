@@ -8,7 +8,6 @@ import sys
 HERE = os.path.dirname(os.path.abspath(__file__))
 sys.path[:0] = [os.path.dirname(HERE), HERE]
 
-import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 from paged_mla_kv_cache_gb300 import workloads as W  # noqa: E402
